@@ -1,0 +1,87 @@
+"""Seeded synthetic inputs for the attention KL divergence.
+
+Shared by the tests, the benchmark and the smoke check; it holds none of the
+method's arithmetic (no scores, softmax or KL), only the recipe that draws the
+teacher and student query/key tensors:
+
+    Q1, K1 ~ N(0, 1) i.i.d. (times ``teacher_scale`` for peaked attention)
+    Q2 = Q1 + sigma * eps_Q,  K2 = K1 + sigma * eps_K,  eps ~ N(0, 1)
+
+drawn in float32 in the order Q1, K1, eps_Q, eps_K from one seeded generator
+and rounded to bf16 (round-to-nearest-even) after the student is formed.  The
+shapes follow the workloads the StreamKL pages evaluate (contexts 4K-512K,
+32 heads, BF16; "Experimental Results").
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    Nq: int
+    Nk: int
+    d: int
+    sigma: float
+    causal: bool
+    teacher_scale: float = 1.0
+    seed: int = 0
+
+    @property
+    def g_value(self) -> float:
+        """Upstream gradient per row: 1 for the tiny case, 1/(H*Nq) otherwise."""
+        return 1.0 if self.name == "tiny" else 1.0 / (self.H * self.Nq)
+
+    def visible_pairs(self) -> int:
+        """Query/key pairs inside the mask, per head.  Causal rows are aligned
+        bottom-right (row i sees keys j <= i + Nk - Nq), so row i sees
+        i + Nk - Nq + 1 keys."""
+        if not self.causal:
+            return self.Nq * self.Nk
+        off = self.Nk - self.Nq
+        return self.Nq * (off + 1) + self.Nq * (self.Nq - 1) // 2
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 1, 2, 256, 256, 64, 0.5, False, seed=0),
+    "8k_causal": Workload("8k_causal", 1, 32, 8192, 8192, 128, 0.3, True, seed=1),
+    "64k_causal": Workload("64k_causal", 1, 32, 65536, 65536, 128, 0.3, True, seed=2),
+    "64k": Workload("64k", 1, 32, 65536, 65536, 128, 0.3, False, seed=2),
+    "decode_q1_k128k": Workload("decode_q1_k128k", 4, 32, 1, 131072, 128, 0.3, False, seed=3),
+    "decode_q16_k128k": Workload("decode_q16_k128k", 4, 32, 16, 131072, 128, 0.3, False, seed=3),
+    "decode_q1_k512k": Workload("decode_q1_k512k", 4, 32, 1, 524288, 128, 0.3, False, seed=3),
+    "decode_q16_k512k": Workload("decode_q16_k512k", 4, 32, 16, 524288, 128, 0.3, False, seed=3),
+    "512k_causal": Workload("512k_causal", 1, 8, 524288, 524288, 128, 0.3, True, teacher_scale=1.5, seed=4),
+}
+
+
+def make_qk(B, H, Nq, Nk, d, sigma, teacher_scale=1.0, seed=0, device="cpu"):
+    """(Q1, K1, Q2, K2) as contiguous bf16 [B, H, N, d] tensors on ``device``."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+
+    def draw(n):
+        return torch.randn((B, H, n, d), generator=gen, device=device, dtype=torch.float32)
+
+    Q1 = draw(Nq)
+    K1 = draw(Nk)
+    if teacher_scale != 1.0:
+        Q1.mul_(teacher_scale)
+        K1.mul_(teacher_scale)
+    Q2 = draw(Nq).mul_(sigma).add_(Q1)
+    K2 = draw(Nk).mul_(sigma).add_(K1)
+    return tuple(t.to(torch.bfloat16).contiguous() for t in (Q1, K1, Q2, K2))
+
+
+def make_workload(w: Workload, device="cpu"):
+    return make_qk(w.B, w.H, w.Nq, w.Nk, w.d, w.sigma, w.teacher_scale, w.seed, device)
+
+
+def make_g(B, H, Nq, value, device="cpu"):
+    """Upstream gradient dL/dKL per row: a constant fill, float32 [B, H, Nq]."""
+    return torch.full((B, H, Nq), float(value), dtype=torch.float32, device=device)
