@@ -1,0 +1,271 @@
+// api.cu -- the C ABI of libstreamkl: argument validation, launch planning,
+// TMA tensor maps and kernel launches on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/streamkl.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace streamkl;
+
+namespace {
+
+constexpr int kMaxSplits = 64;
+constexpr int64_t kDefaultWaitNs = 2000000000LL;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Structural checks that need no device.
+streamkl_status check_shape(const streamkl_shape* s, int causal) {
+    if (!s) return STREAMKL_ERR_INVALID_ARG;
+    if (s->B < 1 || s->H < 1 || s->Nq < 1 || s->Nk < 1 || s->d < 1) return STREAMKL_ERR_INVALID_ARG;
+    if (s->d != 64 && s->d != 128) return STREAMKL_ERR_UNSUPPORTED;
+    if (causal && s->Nq > s->Nk) return STREAMKL_ERR_INVALID_ARG;
+    const int64_t st[6] = {s->q_stride_b, s->q_stride_h, s->q_stride_n, s->k_stride_b, s->k_stride_h, s->k_stride_n};
+    for (int64_t v : st)
+        if (v < 1 || (v % 8) != 0 || v > (int64_t(1) << 38)) return STREAMKL_ERR_INVALID_ARG;
+    if (s->q_stride_n < s->d || s->k_stride_n < s->d) return STREAMKL_ERR_INVALID_ARG;
+    if (int64_t(s->B) * s->H > (int64_t(1) << 24)) return STREAMKL_ERR_UNSUPPORTED;
+    return STREAMKL_OK;
+}
+
+streamkl_status cuda_status(cudaError_t e) { return e == cudaSuccess ? STREAMKL_OK : STREAMKL_ERR_CUDA; }
+
+streamkl_status device_sms(int* sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
+    if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
+    return STREAMKL_OK;
+}
+
+// Key splits for `units` independent rows-tiles of `k_tiles` key tiles each
+// on `slots` resident CTAs: minimise waves * (tiles per split + 1 tile of
+// fixed cost), preferring fewer splits on ties.
+int choose_splits(int64_t units, int k_tiles, int slots) {
+    if (units >= slots || k_tiles < 2) return 1;
+    int best = 1;
+    int64_t best_cost = INT64_MAX;
+    const int smax = k_tiles < kMaxSplits ? k_tiles : kMaxSplits;
+    for (int s = 1; s <= smax; ++s) {
+        const int64_t waves = (units * s + slots - 1) / slots;
+        const int64_t cost = waves * ((k_tiles + s - 1) / s + 1);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
+struct FwdPlan {
+    bool decode;
+    int num_splits;
+    int ctas;
+    int num_q_tiles;
+    int num_k_tiles;
+    size_t ws_bytes;
+};
+
+streamkl_status plan_fwd(const streamkl_shape* s, int causal, const streamkl_options* opt, FwdPlan* pl) {
+    streamkl_status st = check_shape(s, causal);
+    if (st != STREAMKL_OK) return st;
+    if (opt && opt->num_splits < 0) return STREAMKL_ERR_INVALID_ARG;
+    int sms = 0;
+    if ((st = device_sms(&sms)) != STREAMKL_OK) return st;
+    const int64_t BH = int64_t(s->B) * s->H;
+    pl->decode = (s->Nq <= kDecodeMaxQ) && !causal;
+    pl->num_q_tiles = pl->decode ? 1 : (s->Nq + kBlockQ - 1) / kBlockQ;
+    pl->num_k_tiles = (s->Nk + kBlockK - 1) / kBlockK;
+    const int64_t units = BH * pl->num_q_tiles;
+    int splits;
+    if (opt && opt->num_splits > 0)
+        splits = opt->num_splits < pl->num_k_tiles ? opt->num_splits : pl->num_k_tiles;
+    else
+        splits = choose_splits(units, pl->num_k_tiles, sms);
+    if (splits > kMaxSplits) splits = kMaxSplits;
+    const int64_t ctas = units * splits;
+    if (ctas > INT32_MAX) return STREAMKL_ERR_UNSUPPORTED;
+    pl->num_splits = splits;
+    pl->ctas = static_cast<int>(ctas);
+    pl->ws_bytes = kStatusBytes;
+    if (splits > 1) pl->ws_bytes += size_t(5) * splits * size_t(BH) * s->Nq * sizeof(float);
+    return STREAMKL_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 4-D map over [B, H, N, d] bf16 with a (64 x rows) box, 128-byte swizzle;
+// rows outside [0, N) read as zero.
+bool make_map(CUtensorMap* m, const void* ptr, const streamkl_shape* s, bool is_q, int box_rows) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const int64_t N = is_q ? s->Nq : s->Nk;
+    const int64_t sb = is_q ? s->q_stride_b : s->k_stride_b;
+    const int64_t sh = is_q ? s->q_stride_h : s->k_stride_h;
+    const int64_t sn = is_q ? s->q_stride_n : s->k_stride_n;
+    cuuint64_t dims[4] = {cuuint64_t(s->d), cuuint64_t(N), cuuint64_t(s->H), cuuint64_t(s->B)};
+    cuuint64_t strides[3] = {cuuint64_t(sn * 2), cuuint64_t(sh * 2), cuuint64_t(sb * 2)};
+    cuuint32_t box[4] = {cuuint32_t(kSwizzleCols), cuuint32_t(box_rows), 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+float resolve_scale(float scale, int d) {
+    if (!(scale > 0.f) || std::isinf(scale)) return 1.0f / std::sqrt(static_cast<float>(d));
+    return scale;
+}
+
+int64_t wait_limit(const streamkl_options* opt) {
+    return (opt && opt->wait_limit_ns > 0) ? opt->wait_limit_ns : kDefaultWaitNs;
+}
+
+}  // namespace
+
+extern "C" {
+
+int streamkl_version(void) { return 100; }
+
+const char* streamkl_status_string(streamkl_status s) {
+    switch (s) {
+        case STREAMKL_OK: return "ok";
+        case STREAMKL_ERR_INVALID_ARG: return "invalid argument";
+        case STREAMKL_ERR_UNSUPPORTED: return "unsupported configuration";
+        case STREAMKL_ERR_WORKSPACE: return "workspace missing or too small";
+        case STREAMKL_ERR_CUDA: return "CUDA error";
+        case STREAMKL_ERR_TIMEOUT: return "a kernel wait timed out";
+    }
+    return "unknown status";
+}
+
+streamkl_status streamkl_fwd_plan(const streamkl_shape* shape, int causal, const streamkl_options* opt,
+                                  streamkl_plan* plan) {
+    if (!plan) return STREAMKL_ERR_INVALID_ARG;
+    FwdPlan pl{};
+    streamkl_status st = plan_fwd(shape, causal, opt, &pl);
+    if (st != STREAMKL_OK) return st;
+    plan->path = pl.decode ? 1 : 0;
+    plan->num_splits = pl.num_splits;
+    plan->num_ctas = pl.ctas;
+    plan->launches = pl.num_splits > 1 ? 2 : 1;
+    plan->workspace_bytes = pl.ws_bytes;
+    return STREAMKL_OK;
+}
+
+streamkl_status streamkl_fwd(const streamkl_shape* shape, const void* Q1, const void* K1, const void* Q2,
+                             const void* K2, float scale, int causal, float* KL, float* LSE1, float* LSE2,
+                             void* workspace, size_t workspace_bytes, const streamkl_options* opt,
+                             streamkl_stream_t stream) {
+    streamkl_status st = check_shape(shape, causal);
+    if (st != STREAMKL_OK) return st;
+    const void* ptrs[7] = {Q1, K1, Q2, K2, KL, LSE1, LSE2};
+    for (const void* q : ptrs)
+        if (!q) return STREAMKL_ERR_INVALID_ARG;
+    for (int k = 0; k < 4; ++k)
+        if (!aligned16(ptrs[k])) return STREAMKL_ERR_INVALID_ARG;
+    for (int k = 4; k < 7; ++k)
+        if ((reinterpret_cast<uintptr_t>(ptrs[k]) & 3u) != 0) return STREAMKL_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace)) return STREAMKL_ERR_WORKSPACE;
+    FwdPlan pl{};
+    if ((st = plan_fwd(shape, causal, opt, &pl)) != STREAMKL_OK) return st;
+    if (workspace_bytes < pl.ws_bytes) return STREAMKL_ERR_WORKSPACE;
+
+    const int qrows = pl.decode ? kDecodeMaxQ : kBlockQ;
+    CUtensorMap maps[4];
+    if (!make_map(&maps[0], Q1, shape, true, qrows) || !make_map(&maps[1], K1, shape, false, kBlockK) ||
+        !make_map(&maps[2], Q2, shape, true, qrows) || !make_map(&maps[3], K2, shape, false, kBlockK))
+        return STREAMKL_ERR_CUDA;
+
+    const float sc = resolve_scale(scale, shape->d);
+    FwdParams p{};
+    p.B = shape->B;
+    p.H = shape->H;
+    p.Nq = shape->Nq;
+    p.Nk = shape->Nk;
+    p.num_q_tiles = pl.num_q_tiles;
+    p.num_k_tiles = pl.num_k_tiles;
+    p.num_splits = pl.num_splits;
+    p.causal = causal ? 1 : 0;
+    p.diag_off = shape->Nk - shape->Nq;
+    p.scale = sc;
+    p.scale_log2e = sc * 1.4426950408889634f;
+    p.KL = KL;
+    p.LSE1 = LSE1;
+    p.LSE2 = LSE2;
+    p.part = pl.num_splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes) : nullptr;
+    p.status = static_cast<unsigned int*>(workspace);
+    p.wait_ns = static_cast<unsigned long long>(wait_limit(opt));
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = pl.decode ? launch_fwd_decode(shape->d, maps, p, pl.ctas, s)
+                              : launch_fwd_tile(shape->d, maps, p, pl.ctas, s);
+    if (e != cudaSuccess) return STREAMKL_ERR_CUDA;
+    if (pl.num_splits > 1) {
+        CombineParams c{};
+        c.rows = static_cast<int>(int64_t(shape->B) * shape->H * shape->Nq);
+        c.num_splits = pl.num_splits;
+        c.scale = sc;
+        c.scale_log2e = p.scale_log2e;
+        c.part = p.part;
+        c.KL = KL;
+        c.LSE1 = LSE1;
+        c.LSE2 = LSE2;
+        if (launch_combine(c, s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+    }
+    return STREAMKL_OK;
+}
+
+streamkl_status streamkl_bwd_plan(const streamkl_shape* shape, int setting, int causal,
+                                  const streamkl_options* opt, streamkl_plan* plan) {
+    (void)shape;
+    (void)setting;
+    (void)causal;
+    (void)opt;
+    (void)plan;
+    return STREAMKL_ERR_UNSUPPORTED;
+}
+
+streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const float* g, const void* Q1,
+                             const void* K1, const void* Q2, const void* K2, const float* KL, const float* LSE1,
+                             const float* LSE2, float scale, int causal, float* dQ, float* dK, void* workspace,
+                             size_t workspace_bytes, const streamkl_options* opt, streamkl_stream_t stream) {
+    (void)shape; (void)setting; (void)g; (void)Q1; (void)K1; (void)Q2; (void)K2; (void)KL; (void)LSE1;
+    (void)LSE2; (void)scale; (void)causal; (void)dQ; (void)dK; (void)workspace; (void)workspace_bytes;
+    (void)opt; (void)stream;
+    return STREAMKL_ERR_UNSUPPORTED;
+}
+
+streamkl_status streamkl_workspace_status(void* workspace, streamkl_stream_t stream, uint32_t* device_error) {
+    if (!workspace) return STREAMKL_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return STREAMKL_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+    if (word != 0 && cudaMemsetAsync(workspace, 0, sizeof(word), s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+    if (device_error) *device_error = word;
+    return word ? STREAMKL_ERR_TIMEOUT : STREAMKL_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// common.cuh -- tile sizes, kernel parameter blocks and the per-row finish of
+// the online recurrence, shared by the forward, decode, combine and backward
+// kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace streamkl {
+
+constexpr int kBlockQ = 128;        // query rows per tile = TMEM lanes = MMA M
+constexpr int kBlockK = 128;        // keys per tile = MMA N of the score GEMMs
+constexpr int kSwizzleCols = 64;    // bf16 columns per 128-byte swizzled row
+constexpr int kDecodeMaxQ = 16;     // the decode kernel handles Nq <= 16
+constexpr int kStatusBytes = 256;   // workspace prefix holding the error word
+
+// Device error word bits (set by kernels, read by streamkl_workspace_status).
+constexpr uint32_t kErrWaitQ = 1u << 0;      // Q tile never arrived
+constexpr uint32_t kErrWaitK = 1u << 1;      // K tile never arrived / stage never freed
+constexpr uint32_t kErrWaitS = 1u << 2;      // score tile never produced / consumed
+constexpr uint32_t kErrWaitOther = 1u << 3;  // any other barrier
+
+// Forward (tile kernel and decode kernel share this block).
+struct FwdParams {
+    int B, H, Nq, Nk;
+    int num_q_tiles;     // ceil(Nq / q rows per tile)
+    int num_k_tiles;     // ceil(Nk / kBlockK)
+    int num_splits;      // key-range splits per query tile (1 = write final outputs)
+    int causal;          // bottom-right causal mask
+    int diag_off;        // Nk - Nq
+    float scale;         // softmax scale
+    float scale_log2e;   // scale * log2(e): raw dot product -> base-2 exponent
+    float* KL;           // [B*H*Nq]
+    float* LSE1;
+    float* LSE2;
+    float* part;         // partial states [5][num_splits][B*H*Nq] when num_splits > 1
+    unsigned int* status;
+    unsigned long long wait_ns;
+};
+
+// Combine of Split-K partial states.
+struct CombineParams {
+    int rows;            // B*H*Nq
+    int num_splits;
+    float scale;
+    float scale_log2e;
+    const float* part;
+    float* KL;
+    float* LSE1;
+    float* LSE2;
+};
+
+// Partial state of one row over a key range, in the units the kernels keep:
+//   m1, m2  running reference maxima of the raw dot products z = <q, k>
+//   l1, l2  sum_j 2^(c (z_t[j] - m_t)),  c = scale * log2(e)
+//   acc     sum_j 2^(c (z1[j] - m1)) * (z1[j] - z2[j])
+// An empty range has m = -inf and l = acc = 0.
+struct RowState {
+    float m1, l1, acc, m2, l2;
+};
+
+__device__ __forceinline__ void merge_state(RowState& a, const RowState& b, float c) {
+    // log-sum-exp merge; acc follows the teacher maximum only
+    float m1 = fmaxf(a.m1, b.m1), m2 = fmaxf(a.m2, b.m2);
+    float wa1 = (a.m1 == -INFINITY) ? 0.f : exp2f(c * (a.m1 - m1));
+    float wb1 = (b.m1 == -INFINITY) ? 0.f : exp2f(c * (b.m1 - m1));
+    float wa2 = (a.m2 == -INFINITY) ? 0.f : exp2f(c * (a.m2 - m2));
+    float wb2 = (b.m2 == -INFINITY) ? 0.f : exp2f(c * (b.m2 - m2));
+    a.l1 = a.l1 * wa1 + b.l1 * wb1;
+    a.acc = a.acc * wa1 + b.acc * wb1;
+    a.l2 = a.l2 * wa2 + b.l2 * wb2;
+    a.m1 = m1;
+    a.m2 = m2;
+}
+
+// Finish (Methodology 1): LSE_t = scale*m_t + ln l_t and
+// KL = scale * acc / l1 + LSE2 - LSE1.
+__device__ __forceinline__ void finish_row(const RowState& s, float scale, float& kl, float& lse1, float& lse2) {
+    lse1 = scale * s.m1 + logf(s.l1);
+    lse2 = scale * s.m2 + logf(s.l2);
+    kl = scale * (s.acc / s.l1) + (lse2 - lse1);
+}
+
+}  // namespace streamkl

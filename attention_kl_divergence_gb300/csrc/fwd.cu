@@ -1,0 +1,596 @@
+// fwd.cu -- forward kernels of the attention KL divergence on sm_103a.
+//
+//   fwd_tile_kernel   one 128-row query tile x a range of 128-key tiles: both
+//                     score GEMMs on tcgen05 (TMEM accumulators, TMA-staged
+//                     bf16 operands), the five-scalar online update in
+//                     registers, causal tiles beyond the frontier skipped.
+//   fwd_decode_kernel Nq <= 16: keys on the MMA M side (swap of A and B), so
+//                     one CTA streams 128 keys per step for every query; the
+//                     key range is split across CTAs.
+//   combine_kernel    merges the per-split partial states of a row.
+//
+// Method: "StreamKL: Fast and Memory-Efficient KL Divergence for Boosting
+// Attention Distillation" (gist.science/paper/2606.20005, technical summary),
+// Methodology 1 (online formulation: m1, m2, l1, l2, acc with acc rescaled by
+// the teacher maximum; KL = acc/l1 + LSE2 - LSE1) and Methodology 3 (Split-K).
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace streamkl {
+
+namespace {
+
+constexpr float kTau = 8.0f;  // lazy rescale: tolerate running maxima up to 2^8 stale
+
+// Shared-memory plan of the tile kernel.  Every operand tile starts on a
+// 1024-byte boundary (128-byte swizzle atoms of 8 rows).
+template <int D, int NST>
+struct TileSmem {
+    static constexpr int kQBytes = kBlockQ * D * 2;
+    static constexpr int kKBytes = kBlockK * D * 2;
+    static constexpr int q1 = 0;
+    static constexpr int q2 = kQBytes;
+    static constexpr int k = 2 * kQBytes;  // stage s: K1 at k + 2*s*kKBytes, K2 right after
+    static constexpr int bars = k + 2 * NST * kKBytes;
+    // barriers: q_full, k_full[NST], k_empty[NST], s_full[2], s_empty[2]
+    static constexpr int bar_q = bars;
+    static constexpr int bar_kfull = bars + 8;
+    static constexpr int bar_kempty = bar_kfull + 8 * NST;
+    static constexpr int bar_sfull = bar_kempty + 8 * NST;
+    static constexpr int bar_sempty = bar_sfull + 16;
+    static constexpr int misc = bar_sempty + 16;  // tmem base (4 B), abort flag (4 B)
+    static constexpr int total = misc + 16;
+    static constexpr int alloc = total + 1024;    // slack for 1024-byte alignment
+};
+
+__device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
+}
+
+// One 32-column chunk of a score row: online update of the five scalars.
+// MASKED: only columns e <= last are visible (causal frontier or key tail).
+template <bool MASKED>
+__device__ __forceinline__ void update_chunk(const float (&z1)[32], const float (&z2)[32], int last, RowState& st,
+                                             float c, float tau) {
+    if (MASKED && last < 0) return;  // the whole chunk lies beyond the row's last key
+    float cm1 = -INFINITY, cm2 = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        if (!MASKED || e <= last) {
+            cm1 = fmaxf(cm1, z1[e]);
+            cm2 = fmaxf(cm2, z2[e]);
+        }
+    }
+    if (cm1 > st.m1 + tau) {
+        float a = ex2(c * (st.m1 - cm1));  // 0 on the first visible chunk (m1 = -inf)
+        st.l1 *= a;
+        st.acc *= a;
+        st.m1 = cm1;
+    }
+    if (cm2 > st.m2 + tau) {
+        float a = ex2(c * (st.m2 - cm2));
+        st.l2 *= a;
+        st.m2 = cm2;
+    }
+    if (MASKED && st.m1 == -INFINITY) return;  // nothing visible yet
+    const float n1 = -c * st.m1, n2 = -c * st.m2;
+    float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f}, sa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        float p1 = ex2(fmaf(z1[e], c, n1));
+        float p2 = ex2(fmaf(z2[e], c, n2));
+        float df = z1[e] - z2[e];
+        if (MASKED && e > last) {
+            p1 = 0.f;
+            p2 = 0.f;
+            df = 0.f;
+        }
+        s1[e & 3] += p1;
+        s2[e & 3] += p2;
+        sa[e & 3] = fmaf(p1, df, sa[e & 3]);
+    }
+    st.l1 += (s1[0] + s1[1]) + (s1[2] + s1[3]);
+    st.l2 += (s2[0] + s2[1]) + (s2[2] + s2[3]);
+    st.acc += (sa[0] + sa[1]) + (sa[2] + sa[3]);
+}
+
+__device__ __forceinline__ void store_row(const FwdParams& p, size_t row, int split, const RowState& st,
+                                          bool failed) {
+    if (p.num_splits == 1) {
+        float kl, l1, l2;
+        finish_row(st, p.scale, kl, l1, l2);
+        if (failed) kl = l1 = l2 = __int_as_float(0x7fc00000);
+        p.KL[row] = kl;
+        p.LSE1[row] = l1;
+        p.LSE2[row] = l2;
+    } else {
+        const size_t R = static_cast<size_t>(p.B) * p.H * p.Nq;
+        const size_t S = static_cast<size_t>(p.num_splits);
+        float v[5] = {st.m1, st.l1, st.acc, st.m2, st.l2};
+        if (failed) v[1] = v[4] = __int_as_float(0x7fc00000);
+#pragma unroll
+        for (int f = 0; f < 5; ++f) p.part[(f * S + split) * R + row] = v[f];
+    }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Tile forward.  CTA = 6 warps: warp 0 issues TMA, warp 1 owns TMEM and issues
+// the MMAs, warps 2-5 (one per TMEM lane quarter) run the online update, one
+// query row per thread.  TMEM: two buffers x (S1 | S2), 128 columns each.
+// ---------------------------------------------------------------------------
+template <int D, int NST>
+__global__ void __launch_bounds__(192, 1)
+    fwd_tile_kernel(const __grid_constant__ CUtensorMap tQ1, const __grid_constant__ CUtensorMap tK1,
+                    const __grid_constant__ CUtensorMap tQ2, const __grid_constant__ CUtensorMap tK2,
+                    const FwdParams p) {
+    using L = TileSmem<D, NST>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - smem_u32(smem_raw));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::misc + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::misc);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // ---- which (query tile, head, split) this CTA owns; causal: heaviest first
+    const int BH = p.B * p.H;
+    const int per_q = BH * p.num_splits;
+    const int qi = blockIdx.x / per_q;
+    const int rem = blockIdx.x - qi * per_q;
+    const int bh = rem / p.num_splits;
+    const int split = rem - bh * p.num_splits;
+    const int qt = p.causal ? (p.num_q_tiles - 1 - qi) : qi;
+    const int b = bh / p.H, h = bh - b * p.H;
+    const int q0 = qt * kBlockQ;
+    const int q_last = min(q0 + kBlockQ, p.Nq) - 1;
+    const int kt_total = p.causal ? min(p.num_k_tiles, (q_last + p.diag_off) / kBlockK + 1) : p.num_k_tiles;
+    const int per_split = (kt_total + p.num_splits - 1) / p.num_splits;
+    const int kt_begin = split * per_split;
+    const int n_tiles = max(0, min(kt_total, kt_begin + per_split) - kt_begin);
+
+    if (threadIdx.x == 0) {
+        mbar_init(base + L::bar_q, 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(base + L::bar_kfull + 8 * s, 1);
+            mbar_init(base + L::bar_kempty + 8 * s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(base + L::bar_sfull + 8 * s, 1);
+            mbar_init(base + L::bar_sempty + 8 * s, 128);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) tmem_alloc(base + L::misc, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{abort_flag, p.status, p.wait_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0 && n_tiles > 0) {
+            prefetch_tensormap(&tQ1);
+            prefetch_tensormap(&tK1);
+            prefetch_tensormap(&tQ2);
+            prefetch_tensormap(&tK2);
+            const uint64_t keep = policy_evict_last();  // K tiles are re-read by every query tile
+            mbar_arrive_expect_tx(base + L::bar_q, 2 * L::kQBytes);
+#pragma unroll
+            for (int c = 0; c < D / kSwizzleCols; ++c) {
+                tma_load_4d(base + L::q1 + c * kBlockQ * 128, &tQ1, base + L::bar_q, c * kSwizzleCols, q0, h, b);
+                tma_load_4d(base + L::q2 + c * kBlockQ * 128, &tQ2, base + L::bar_q, c * kSwizzleCols, q0, h, b);
+            }
+            int it = 0;
+            for (; it < n_tiles; ++it) {
+                const int s = it % NST;
+                if (!mbar_wait(base + L::bar_kempty + 8 * s, ((it / NST) & 1) ^ 1, wc, kErrWaitK)) break;
+                const uint32_t fb = base + L::bar_kfull + 8 * s;
+                mbar_arrive_expect_tx(fb, 2 * L::kKBytes);
+                const int k0 = (kt_begin + it) * kBlockK;
+                const uint32_t k1s = base + L::k + 2 * s * L::kKBytes, k2s = k1s + L::kKBytes;
+#pragma unroll
+                for (int c = 0; c < D / kSwizzleCols; ++c) {
+                    tma_load_4d_hint(k1s + c * kBlockK * 128, &tK1, fb, c * kSwizzleCols, k0, h, b, keep);
+                    tma_load_4d_hint(k2s + c * kBlockK * 128, &tK2, fb, c * kSwizzleCols, k0, h, b, keep);
+                }
+            }
+            // drain: every issued copy has landed and every stage was released
+            for (int j = max(0, it - NST); j < it; ++j) {
+                drain_wait(base + L::bar_kfull + 8 * (j % NST), (j / NST) & 1, p.wait_ns);
+                drain_wait(base + L::bar_kempty + 8 * (j % NST), (j / NST) & 1, p.wait_ns / 8 + 1000000);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0 && n_tiles > 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kBlockQ, kBlockK);
+            int issued = 0;
+            if (mbar_wait(base + L::bar_q, 0, wc, kErrWaitQ)) {
+                tc_fence_after();
+                for (int it = 0; it < n_tiles; ++it) {
+                    const int s = it % NST, buf = it & 1;
+                    if (!mbar_wait(base + L::bar_kfull + 8 * s, (it / NST) & 1, wc, kErrWaitK)) break;
+                    if (!mbar_wait(base + L::bar_sempty + 8 * buf, ((it >> 1) & 1) ^ 1, wc, kErrWaitS)) break;
+                    tc_fence_after();
+                    const uint32_t d1 = tmem + buf * 2 * kBlockK, d2 = d1 + kBlockK;
+                    const uint32_t k1s = base + L::k + 2 * s * L::kKBytes, k2s = k1s + L::kKBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t qo = (kk >> 2) * kBlockQ * 128 + (kk & 3) * 32;
+                        const uint32_t ko = (kk >> 2) * kBlockK * 128 + (kk & 3) * 32;
+                        tc_mma_bf16(d1, smem_desc_k128(base + L::q1 + qo), smem_desc_k128(k1s + ko), idesc, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t qo = (kk >> 2) * kBlockQ * 128 + (kk & 3) * 32;
+                        const uint32_t ko = (kk >> 2) * kBlockK * 128 + (kk & 3) * 32;
+                        tc_mma_bf16(d2, smem_desc_k128(base + L::q2 + qo), smem_desc_k128(k2s + ko), idesc, kk > 0);
+                    }
+                    tc_commit(base + L::bar_sfull + 8 * buf);
+                    tc_commit(base + L::bar_kempty + 8 * s);
+                    ++issued;
+                }
+            }
+            if (*abort_flag && issued > 0) {  // let the last MMAs retire before TMEM is freed
+                const int j = issued - 1;
+                drain_wait(base + L::bar_sfull + 8 * (j & 1), (j >> 1) & 1, p.wait_ns);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ online update
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;
+        const int i = q0 + row;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const float c = p.scale_log2e;
+        const float tau = kTau / c;
+        const int limit = p.causal ? min(i + p.diag_off, p.Nk - 1) : p.Nk - 1;  // last visible key
+        RowState st{-INFINITY, 0.f, 0.f, -INFINITY, 0.f};
+        bool ok = true;
+        for (int it = 0; it < n_tiles; ++it) {
+            const int buf = it & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(base + L::bar_sfull + 8 * buf, (it >> 1) & 1, wc, kErrWaitS))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int jrem = limit - (kt_begin + it) * kBlockK;  // last visible column of this tile
+            const uint32_t t1 = tl + buf * 2 * kBlockK, t2 = t1 + kBlockK;
+#pragma unroll 1
+            for (int ch = 0; ch < kBlockK / 32; ++ch) {
+                float z1[32], z2[32];
+                tmem_ld32(t1 + ch * 32, z1);
+                tmem_ld32(t2 + ch * 32, z2);
+                tc_wait_ld();
+                if (ch == kBlockK / 32 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(base + L::bar_sempty + 8 * buf);
+                }
+                const int last = jrem - ch * 32;
+                if (last >= 31)
+                    update_chunk<false>(z1, z2, 31, st, c, tau);
+                else
+                    update_chunk<true>(z1, z2, last, st, c, tau);
+            }
+        }
+        if (i < p.Nq) store_row(p, static_cast<size_t>(bh) * p.Nq + i, split, st, !ok || *abort_flag);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Decode forward, Nq <= 16, no mask.  S^T = K Q^T: M = 128 keys (TMEM lanes),
+// N = 16 query columns.  Each thread owns one key per step and keeps a running
+// state per query; the 128 states are merged at the end of the key range.
+// ---------------------------------------------------------------------------
+template <int D, int NST>
+struct DecodeSmem {
+    static constexpr int kQBytes = kDecodeMaxQ * D * 2;  // 16 rows
+    static constexpr int kKBytes = kBlockK * D * 2;
+    static constexpr int q1 = 0;
+    static constexpr int q2 = ((kQBytes + 1023) / 1024) * 1024;
+    static constexpr int k = q2 + q2;
+    static constexpr int bars = k + 2 * NST * kKBytes;
+    static constexpr int bar_q = bars;
+    static constexpr int bar_kfull = bars + 8;
+    static constexpr int bar_kempty = bar_kfull + 8 * NST;
+    static constexpr int bar_sfull = bar_kempty + 8 * NST;
+    static constexpr int bar_sempty = bar_sfull + 16;
+    static constexpr int misc = bar_sempty + 16;
+    static constexpr int red = misc + 16;                    // [4 warps][16 q][5] floats
+    static constexpr int total = red + 4 * kDecodeMaxQ * 5 * 4;
+    static constexpr int alloc = total + 1024;
+};
+
+template <int D, int NST>
+__global__ void __launch_bounds__(192, 1)
+    fwd_decode_kernel(const __grid_constant__ CUtensorMap tQ1, const __grid_constant__ CUtensorMap tK1,
+                      const __grid_constant__ CUtensorMap tQ2, const __grid_constant__ CUtensorMap tK2,
+                      const FwdParams p) {
+    using L = DecodeSmem<D, NST>;
+    constexpr int NQ = kDecodeMaxQ;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - smem_u32(smem_raw));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::misc + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::misc);
+    float* red = reinterpret_cast<float*>(gbase + L::red);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x / p.num_splits;
+    const int split = blockIdx.x - bh * p.num_splits;
+    const int b = bh / p.H, h = bh - b * p.H;
+    const int per_split = (p.num_k_tiles + p.num_splits - 1) / p.num_splits;
+    const int kt_begin = split * per_split;
+    const int n_tiles = max(0, min(p.num_k_tiles, kt_begin + per_split) - kt_begin);
+
+    if (threadIdx.x == 0) {
+        mbar_init(base + L::bar_q, 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(base + L::bar_kfull + 8 * s, 1);
+            mbar_init(base + L::bar_kempty + 8 * s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(base + L::bar_sfull + 8 * s, 1);
+            mbar_init(base + L::bar_sempty + 8 * s, 128);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) tmem_alloc(base + L::misc, 64);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{abort_flag, p.status, p.wait_ns};
+
+    if (warp == 0) {
+        if (lane == 0 && n_tiles > 0) {
+            prefetch_tensormap(&tQ1);
+            prefetch_tensormap(&tK1);
+            prefetch_tensormap(&tQ2);
+            prefetch_tensormap(&tK2);
+            const uint64_t stream_once = policy_evict_first();  // each key is read exactly once
+            mbar_arrive_expect_tx(base + L::bar_q, 2 * L::kQBytes);
+#pragma unroll
+            for (int c = 0; c < D / kSwizzleCols; ++c) {
+                tma_load_4d(base + L::q1 + c * NQ * 128, &tQ1, base + L::bar_q, c * kSwizzleCols, 0, h, b);
+                tma_load_4d(base + L::q2 + c * NQ * 128, &tQ2, base + L::bar_q, c * kSwizzleCols, 0, h, b);
+            }
+            int it = 0;
+            for (; it < n_tiles; ++it) {
+                const int s = it % NST;
+                if (!mbar_wait(base + L::bar_kempty + 8 * s, ((it / NST) & 1) ^ 1, wc, kErrWaitK)) break;
+                const uint32_t fb = base + L::bar_kfull + 8 * s;
+                mbar_arrive_expect_tx(fb, 2 * L::kKBytes);
+                const int k0 = (kt_begin + it) * kBlockK;
+                const uint32_t k1s = base + L::k + 2 * s * L::kKBytes, k2s = k1s + L::kKBytes;
+#pragma unroll
+                for (int c = 0; c < D / kSwizzleCols; ++c) {
+                    tma_load_4d_hint(k1s + c * kBlockK * 128, &tK1, fb, c * kSwizzleCols, k0, h, b, stream_once);
+                    tma_load_4d_hint(k2s + c * kBlockK * 128, &tK2, fb, c * kSwizzleCols, k0, h, b, stream_once);
+                }
+            }
+            for (int j = max(0, it - NST); j < it; ++j) {
+                drain_wait(base + L::bar_kfull + 8 * (j % NST), (j / NST) & 1, p.wait_ns);
+                drain_wait(base + L::bar_kempty + 8 * (j % NST), (j / NST) & 1, p.wait_ns / 8 + 1000000);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && n_tiles > 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kBlockK, NQ);
+            int issued = 0;
+            if (mbar_wait(base + L::bar_q, 0, wc, kErrWaitQ)) {
+                tc_fence_after();
+                for (int it = 0; it < n_tiles; ++it) {
+                    const int s = it % NST, buf = it & 1;
+                    if (!mbar_wait(base + L::bar_kfull + 8 * s, (it / NST) & 1, wc, kErrWaitK)) break;
+                    if (!mbar_wait(base + L::bar_sempty + 8 * buf, ((it >> 1) & 1) ^ 1, wc, kErrWaitS)) break;
+                    tc_fence_after();
+                    const uint32_t d1 = tmem + buf * 2 * NQ, d2 = d1 + NQ;
+                    const uint32_t k1s = base + L::k + 2 * s * L::kKBytes, k2s = k1s + L::kKBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ko = (kk >> 2) * kBlockK * 128 + (kk & 3) * 32;
+                        const uint32_t qo = (kk >> 2) * NQ * 128 + (kk & 3) * 32;
+                        tc_mma_bf16(d1, smem_desc_k128(k1s + ko), smem_desc_k128(base + L::q1 + qo), idesc, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ko = (kk >> 2) * kBlockK * 128 + (kk & 3) * 32;
+                        const uint32_t qo = (kk >> 2) * NQ * 128 + (kk & 3) * 32;
+                        tc_mma_bf16(d2, smem_desc_k128(k2s + ko), smem_desc_k128(base + L::q2 + qo), idesc, kk > 0);
+                    }
+                    tc_commit(base + L::bar_sfull + 8 * buf);
+                    tc_commit(base + L::bar_kempty + 8 * s);
+                    ++issued;
+                }
+            }
+            if (*abort_flag && issued > 0) {
+                const int j = issued - 1;
+                drain_wait(base + L::bar_sfull + 8 * (j & 1), (j >> 1) & 1, p.wait_ns);
+            }
+        }
+    } else {
+        const int wq = warp & 3;
+        const int krow = wq * 32 + lane;  // key within the tile = TMEM lane
+        const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const float c = p.scale_log2e;
+        const float tau = kTau / c;
+        const int nq = p.Nq;
+        float m1[NQ], l1[NQ], ac[NQ], m2[NQ], l2[NQ];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            m1[q] = -INFINITY;
+            m2[q] = -INFINITY;
+            l1[q] = l2[q] = ac[q] = 0.f;
+        }
+        bool ok = true;
+        for (int it = 0; it < n_tiles; ++it) {
+            const int buf = it & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(base + L::bar_sfull + 8 * buf, (it >> 1) & 1, wc, kErrWaitS))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float z1[NQ], z2[NQ];
+            tmem_ld16(tl + buf * 2 * NQ, z1);
+            tmem_ld16(tl + buf * 2 * NQ + NQ, z2);
+            tc_wait_ld();
+            tc_fence_before();
+            mbar_arrive(base + L::bar_sempty + 8 * buf);
+            if ((kt_begin + it) * kBlockK + krow >= p.Nk) continue;  // key tail
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                if (q < nq) {
+                    if (z1[q] > m1[q] + tau) {
+                        const float a = ex2(c * (m1[q] - z1[q]));
+                        l1[q] *= a;
+                        ac[q] *= a;
+                        m1[q] = z1[q];
+                    }
+                    if (z2[q] > m2[q] + tau) {
+                        l2[q] *= ex2(c * (m2[q] - z2[q]));
+                        m2[q] = z2[q];
+                    }
+                    const float p1 = ex2(c * (z1[q] - m1[q]));
+                    l1[q] += p1;
+                    ac[q] = fmaf(p1, z1[q] - z2[q], ac[q]);
+                    l2[q] += ex2(c * (z2[q] - m2[q]));
+                }
+            }
+        }
+        // merge the 128 per-key states of every query: warp butterfly, then warps
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            if (q < nq) {
+                RowState s{m1[q], l1[q], ac[q], m2[q], l2[q]};
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    RowState t{__shfl_xor_sync(0xffffffffu, s.m1, o), __shfl_xor_sync(0xffffffffu, s.l1, o),
+                               __shfl_xor_sync(0xffffffffu, s.acc, o), __shfl_xor_sync(0xffffffffu, s.m2, o),
+                               __shfl_xor_sync(0xffffffffu, s.l2, o)};
+                    merge_state(s, t, c);
+                }
+                if (lane == 0) {
+                    float* r = red + (wq * NQ + q) * 5;
+                    r[0] = s.m1;
+                    r[1] = s.l1;
+                    r[2] = s.acc;
+                    r[3] = s.m2;
+                    r[4] = s.l2;
+                }
+            }
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four update warps only
+        if (wq == 0 && lane < nq) {
+            const int q = lane;
+            RowState s{-INFINITY, 0.f, 0.f, -INFINITY, 0.f};
+            for (int w = 0; w < 4; ++w) {
+                const float* r = red + (w * NQ + q) * 5;
+                RowState t{r[0], r[1], r[2], r[3], r[4]};
+                merge_state(s, t, c);
+            }
+            store_row(p, static_cast<size_t>(bh) * p.Nq + q, split, s, !ok || *abort_flag);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 64);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Split-K combine: one thread per row merges its partial states and finishes.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) combine_kernel(const CombineParams p) {
+    const int row = blockIdx.x * blockDim.x + threadIdx.x;
+    if (row >= p.rows) return;
+    const size_t R = static_cast<size_t>(p.rows);
+    const size_t S = static_cast<size_t>(p.num_splits);
+    RowState s{-INFINITY, 0.f, 0.f, -INFINITY, 0.f};
+    for (int k = 0; k < p.num_splits; ++k) {
+        RowState t{p.part[(0 * S + k) * R + row], p.part[(1 * S + k) * R + row], p.part[(2 * S + k) * R + row],
+                   p.part[(3 * S + k) * R + row], p.part[(4 * S + k) * R + row]};
+        merge_state(s, t, p.scale_log2e);
+    }
+    float kl, l1, l2;
+    finish_row(s, p.scale, kl, l1, l2);
+    p.KL[row] = kl;
+    p.LSE1[row] = l1;
+    p.LSE2[row] = l2;
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launchers
+// ---------------------------------------------------------------------------
+namespace {
+template <typename K>
+cudaError_t ensure_smem(K kernel, int bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+}  // namespace
+
+cudaError_t launch_fwd_tile(int d, const CUtensorMap* maps, const FwdParams& p, int ctas, cudaStream_t stream) {
+    cudaError_t e;
+    if (d == 128) {
+        constexpr int NST = 2;
+        auto k = fwd_tile_kernel<128, NST>;
+        if ((e = ensure_smem(k, TileSmem<128, NST>::alloc)) != cudaSuccess) return e;
+        k<<<ctas, 192, TileSmem<128, NST>::alloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+    } else {
+        constexpr int NST = 4;
+        auto k = fwd_tile_kernel<64, NST>;
+        if ((e = ensure_smem(k, TileSmem<64, NST>::alloc)) != cudaSuccess) return e;
+        k<<<ctas, 192, TileSmem<64, NST>::alloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_decode(int d, const CUtensorMap* maps, const FwdParams& p, int ctas, cudaStream_t stream) {
+    cudaError_t e;
+    if (d == 128) {
+        constexpr int NST = 3;
+        auto k = fwd_decode_kernel<128, NST>;
+        if ((e = ensure_smem(k, DecodeSmem<128, NST>::alloc)) != cudaSuccess) return e;
+        k<<<ctas, 192, DecodeSmem<128, NST>::alloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+    } else {
+        constexpr int NST = 6;
+        auto k = fwd_decode_kernel<64, NST>;
+        if ((e = ensure_smem(k, DecodeSmem<64, NST>::alloc)) != cudaSuccess) return e;
+        k<<<ctas, 192, DecodeSmem<64, NST>::alloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
+    const int threads = 256;
+    combine_kernel<<<(p.rows + threads - 1) / threads, threads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+int fwd_tile_stages(int d) { return d == 128 ? 2 : 4; }
+
+}  // namespace streamkl

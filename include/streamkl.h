@@ -1,0 +1,143 @@
+/*
+ * streamkl.h -- C ABI of libstreamkl: the fused attention KL divergence on
+ * one GB300 (sm_103a) GPU.
+ *
+ * Method: "StreamKL: Fast and Memory-Efficient KL Divergence for Boosting
+ * Attention Distillation" (gist.science/paper/2606.20005, technical summary).
+ * For every query row i of every (batch b, head h):
+ *
+ *     S_t = scale * Q_t K_t^T        t = 1 (teacher), 2 (student)
+ *     P_t = softmax(S_t) over the keys row i may see
+ *     KL[i] = sum_j P1[i,j] * (log P1[i,j] - log P2[i,j])        (Problem Statement)
+ *
+ * computed without ever holding an Nq x Nk matrix: the forward streams key
+ * tiles through five running scalars per row (Methodology 1, "Online
+ * Formulation") and saves only KL, LSE1, LSE2; the backward regenerates
+ * P_t = exp(S_t - LSE_t) tile by tile (Methodology 2, "Recomputation
+ * Strategy").  Small query counts split the key range across CTAs and merge
+ * the partial states (Methodology 3, "Split-K Variant").
+ *
+ * Conventions shared by every entry point
+ *  - Q1, K1, Q2, K2 are bf16 device tensors laid out [B, H, N, d] with d
+ *    contiguous; the element strides of the B, H and N axes are given in
+ *    streamkl_shape and must be multiples of 8 elements (16 bytes).  Q1 and
+ *    Q2 share one set of strides, K1 and K2 another.  Base pointers must be
+ *    16-byte aligned.  d must be 64 or 128.
+ *  - KL, LSE1, LSE2 and g are float32 [B, H, Nq], contiguous.  dQ is float32
+ *    [B, H, Nq, d] and dK float32 [B, H, Nk, d], contiguous.
+ *  - Logarithms are natural.  LSE_t[i] = log sum_j exp(S_t[i,j]) includes the
+ *    softmax scale.
+ *  - causal != 0 aligns the mask bottom-right: row i sees keys
+ *    j <= i + (Nk - Nq).  It requires Nq <= Nk, so no row is empty.
+ *  - scale <= 0 (or NaN) selects the default d^-1/2.
+ *  - The caller owns every buffer, inputs, outputs and workspace alike.  The
+ *    library allocates no device memory, keeps no state between calls and
+ *    runs everything asynchronously on the caller's stream.  Arguments are
+ *    validated before anything is launched; on an error nothing is launched
+ *    and no output is touched.
+ *  - Workspace: the first 256 bytes hold a device error word that kernels set
+ *    (they never clear it) when a bounded wait inside them gives up.  Zero the
+ *    workspace once when it is allocated; streamkl_workspace_status reads and
+ *    clears the word.  A workspace must not be shared by calls that may run
+ *    at the same time on different streams.
+ */
+#ifndef STREAMKL_H
+#define STREAMKL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define STREAMKL_API __attribute__((visibility("default")))
+#else
+#define STREAMKL_API
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* streamkl_stream_t;
+
+typedef enum {
+    STREAMKL_OK = 0,
+    STREAMKL_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, bad setting */
+    STREAMKL_ERR_UNSUPPORTED = 2, /* valid but not implemented here (e.g. d not 64/128) */
+    STREAMKL_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the size query said */
+    STREAMKL_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
+    STREAMKL_ERR_TIMEOUT = 5      /* a kernel's bounded wait gave up (device error word) */
+} streamkl_status;
+
+typedef struct {
+    int32_t B, H, Nq, Nk, d;
+    int64_t q_stride_b, q_stride_h, q_stride_n; /* element strides of Q1 and Q2 */
+    int64_t k_stride_b, k_stride_h, k_stride_n; /* element strides of K1 and K2 */
+} streamkl_shape;
+
+/* Optional knobs; pass NULL for the defaults. */
+typedef struct {
+    int32_t num_splits;    /* forward: 0 = automatic, n >= 1 forces n key splits     */
+    int32_t bwd_mode;      /* backward: 0 = automatic, 1 = fused (atomic dQ),        */
+                           /*           2 = separate dQ and dK kernels                */
+    int64_t wait_limit_ns; /* limit of every in-kernel wait; 0 = default (2 s)      */
+} streamkl_options;
+
+/* What a call will launch for a given shape (filled by the plan queries). */
+typedef struct {
+    int32_t path;       /* 0 = tile forward, 1 = decode (Nq <= 16) forward,
+                           2 = fused backward, 3 = separate-kernel backward */
+    int32_t num_splits; /* key splits of the forward (1 = no combine step)  */
+    int32_t num_ctas;   /* CTAs of the main kernel                          */
+    int32_t launches;   /* kernels launched per call                        */
+    size_t workspace_bytes;
+} streamkl_plan;
+
+/* Plan of streamkl_fwd for this shape on the current device.  Needs a CUDA
+ * device (the split count depends on its SM count).  Errors: INVALID_ARG,
+ * UNSUPPORTED, CUDA. */
+STREAMKL_API streamkl_status streamkl_fwd_plan(const streamkl_shape* shape, int causal, const streamkl_options* opt,
+                                  streamkl_plan* plan);
+
+/* Forward (Methodology 1 and 3).  Writes KL, LSE1, LSE2 for every row.
+ * workspace must hold at least streamkl_fwd_plan(...).workspace_bytes bytes
+ * (256 for the status word plus 20 bytes per row and split when the key
+ * range is split).  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+STREAMKL_API streamkl_status streamkl_fwd(const streamkl_shape* shape, const void* Q1, const void* K1, const void* Q2,
+                             const void* K2, float scale, int causal, float* KL, float* LSE1, float* LSE2,
+                             void* workspace, size_t workspace_bytes, const streamkl_options* opt,
+                             streamkl_stream_t stream);
+
+/* Plan of streamkl_bwd (fused vs separate kernels, workspace). */
+STREAMKL_API streamkl_status streamkl_bwd_plan(const streamkl_shape* shape, int setting, int causal,
+                                  const streamkl_options* opt, streamkl_plan* plan);
+
+/* Backward (Methodology 2).  Gradient of sum_i g[i] * KL[i] with respect to
+ * the trainable side:
+ *   setting 1 (teacher fixed): dQ = dL/dQ2, dK = dL/dK2, dS2 = g (P2 - P1)
+ *   setting 2 (student fixed): dQ = dL/dQ1, dK = dL/dK1,
+ *                              dS1 = g P1 ((S1 - LSE1) - (S2 - LSE2) - KL)
+ * and dQ = scale * dS K, dK = scale * dS^T Q.  KL, LSE1, LSE2 are the
+ * forward's outputs for the same inputs.  dQ and dK are overwritten.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+STREAMKL_API streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const float* g, const void* Q1,
+                             const void* K1, const void* Q2, const void* K2, const float* KL, const float* LSE1,
+                             const float* LSE2, float scale, int causal, float* dQ, float* dK, void* workspace,
+                             size_t workspace_bytes, const streamkl_options* opt, streamkl_stream_t stream);
+
+/* Synchronises `stream`, reads the workspace's device error word into
+ * *device_error (if not NULL), clears it, and returns STREAMKL_ERR_TIMEOUT if
+ * it was set, STREAMKL_OK otherwise (or CUDA on a failed copy). */
+STREAMKL_API streamkl_status streamkl_workspace_status(void* workspace, streamkl_stream_t stream, uint32_t* device_error);
+
+/* Static description of a status code; never NULL. */
+STREAMKL_API const char* streamkl_status_string(streamkl_status status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+STREAMKL_API int streamkl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STREAMKL_H */
