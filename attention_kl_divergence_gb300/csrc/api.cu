@@ -36,8 +36,6 @@ streamkl_status check_shape(const streamkl_shape* s, int causal) {
     return STREAMKL_OK;
 }
 
-streamkl_status cuda_status(cudaError_t e) { return e == cudaSuccess ? STREAMKL_OK : STREAMKL_ERR_CUDA; }
-
 streamkl_status device_sms(int* sms) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
@@ -96,6 +94,42 @@ streamkl_status plan_fwd(const streamkl_shape* s, int causal, const streamkl_opt
     pl->ctas = static_cast<int>(ctas);
     pl->ws_bytes = kStatusBytes;
     if (splits > 1) pl->ws_bytes += size_t(5) * splits * size_t(BH) * s->Nq * sizeof(float);
+    return STREAMKL_OK;
+}
+
+struct BwdPlan {
+    bool fused;
+    int ctas_q;
+    int ctas_kv;
+    size_t ws_bytes;
+};
+
+// Fused mode (one kernel, dQ through atomics) when the float32 dQ buffer fits
+// in L2 ("atomics for dQ when the buffer fits in L2"), else the two-kernel
+// split.  The fused kernel's dQ^T tile needs d = 128.
+streamkl_status plan_bwd(const streamkl_shape* s, int setting, int causal, const streamkl_options* opt,
+                         BwdPlan* pl) {
+    streamkl_status st = check_shape(s, causal);
+    if (st != STREAMKL_OK) return st;
+    if (setting != 1 && setting != 2) return STREAMKL_ERR_INVALID_ARG;
+    const int mode = opt ? opt->bwd_mode : 0;
+    if (mode < 0 || mode > 2) return STREAMKL_ERR_INVALID_ARG;
+    if (mode == 1 && s->d != 128) return STREAMKL_ERR_UNSUPPORTED;
+    int dev = 0, l2 = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
+    const int64_t BH = int64_t(s->B) * s->H;
+    const double dq_bytes = double(BH) * s->Nq * s->d * 4.0;
+    if (mode == 0)
+        pl->fused = s->d == 128 && dq_bytes <= double(l2);
+    else
+        pl->fused = mode == 1;
+    const int64_t ctas_kv = BH * ((s->Nk + kBlockK - 1) / kBlockK);
+    const int64_t ctas_q = BH * ((s->Nq + kBlockQ - 1) / kBlockQ);
+    if (ctas_kv > INT32_MAX || ctas_q > INT32_MAX) return STREAMKL_ERR_UNSUPPORTED;
+    pl->ctas_kv = static_cast<int>(ctas_kv);
+    pl->ctas_q = static_cast<int>(ctas_q);
+    pl->ws_bytes = kStatusBytes;
     return STREAMKL_OK;
 }
 
@@ -238,22 +272,82 @@ streamkl_status streamkl_fwd(const streamkl_shape* shape, const void* Q1, const 
 
 streamkl_status streamkl_bwd_plan(const streamkl_shape* shape, int setting, int causal,
                                   const streamkl_options* opt, streamkl_plan* plan) {
-    (void)shape;
-    (void)setting;
-    (void)causal;
-    (void)opt;
-    (void)plan;
-    return STREAMKL_ERR_UNSUPPORTED;
+    if (!plan) return STREAMKL_ERR_INVALID_ARG;
+    BwdPlan pl{};
+    streamkl_status st = plan_bwd(shape, setting, causal, opt, &pl);
+    if (st != STREAMKL_OK) return st;
+    plan->path = pl.fused ? 2 : 3;
+    plan->num_splits = 1;
+    plan->num_ctas = pl.ctas_kv;
+    plan->launches = 2;  // fused: zero dQ + kernel; split: two kernels
+    plan->workspace_bytes = pl.ws_bytes;
+    return STREAMKL_OK;
 }
 
 streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const float* g, const void* Q1,
                              const void* K1, const void* Q2, const void* K2, const float* KL, const float* LSE1,
                              const float* LSE2, float scale, int causal, float* dQ, float* dK, void* workspace,
                              size_t workspace_bytes, const streamkl_options* opt, streamkl_stream_t stream) {
-    (void)shape; (void)setting; (void)g; (void)Q1; (void)K1; (void)Q2; (void)K2; (void)KL; (void)LSE1;
-    (void)LSE2; (void)scale; (void)causal; (void)dQ; (void)dK; (void)workspace; (void)workspace_bytes;
-    (void)opt; (void)stream;
-    return STREAMKL_ERR_UNSUPPORTED;
+    streamkl_status st = check_shape(shape, causal);
+    if (st != STREAMKL_OK) return st;
+    if (setting != 1 && setting != 2) return STREAMKL_ERR_INVALID_ARG;
+    const void* qk[4] = {Q1, K1, Q2, K2};
+    for (const void* q : qk)
+        if (!q || !aligned16(q)) return STREAMKL_ERR_INVALID_ARG;
+    const void* rows[4] = {g, KL, LSE1, LSE2};
+    for (const void* q : rows)
+        if (!q || (reinterpret_cast<uintptr_t>(q) & 3u) != 0) return STREAMKL_ERR_INVALID_ARG;
+    if (!dQ || !dK || !aligned16(dQ) || !aligned16(dK)) return STREAMKL_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace)) return STREAMKL_ERR_WORKSPACE;
+    BwdPlan pl{};
+    if ((st = plan_bwd(shape, setting, causal, opt, &pl)) != STREAMKL_OK) return st;
+    if (workspace_bytes < pl.ws_bytes) return STREAMKL_ERR_WORKSPACE;
+
+    const float sc = resolve_scale(scale, shape->d);
+    BwdParams p{};
+    p.B = shape->B;
+    p.H = shape->H;
+    p.Nq = shape->Nq;
+    p.Nk = shape->Nk;
+    p.causal = causal ? 1 : 0;
+    p.diag_off = shape->Nk - shape->Nq;
+    p.scale = sc;
+    p.scale_log2e = sc * 1.4426950408889634f;
+    p.g = g;
+    p.KL = KL;
+    p.LSE1 = LSE1;
+    p.LSE2 = LSE2;
+    p.dQ = dQ;
+    p.dK = dK;
+    p.status = static_cast<unsigned int*>(workspace);
+    p.wait_ns = static_cast<unsigned long long>(wait_limit(opt));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    // key-tile kernel: Q boxes of 64 rows, K boxes of 128 rows
+    CUtensorMap kv[4];
+    if (!make_map(&kv[0], Q1, shape, true, 64) || !make_map(&kv[1], K1, shape, false, kBlockK) ||
+        !make_map(&kv[2], Q2, shape, true, 64) || !make_map(&kv[3], K2, shape, false, kBlockK))
+        return STREAMKL_ERR_CUDA;
+    BwdParams pkv = p;
+    pkv.num_q_tiles = (shape->Nq + 63) / 64;
+    pkv.num_k_tiles = (shape->Nk + kBlockK - 1) / kBlockK;
+    if (pl.fused) {
+        const size_t dq_bytes = size_t(shape->B) * shape->H * shape->Nq * shape->d * sizeof(float);
+        if (cudaMemsetAsync(dQ, 0, dq_bytes, s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+        if (launch_bwd_kv(shape->d, setting, true, kv, pkv, pl.ctas_kv, s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+        return STREAMKL_OK;
+    }
+    // query-tile kernel: Q boxes of 128 rows, K boxes of 64 rows
+    CUtensorMap qm[4];
+    if (!make_map(&qm[0], Q1, shape, true, kBlockQ) || !make_map(&qm[1], K1, shape, false, 64) ||
+        !make_map(&qm[2], Q2, shape, true, kBlockQ) || !make_map(&qm[3], K2, shape, false, 64))
+        return STREAMKL_ERR_CUDA;
+    BwdParams pq = p;
+    pq.num_q_tiles = (shape->Nq + kBlockQ - 1) / kBlockQ;
+    pq.num_k_tiles = (shape->Nk + 63) / 64;
+    if (launch_bwd_q(shape->d, setting, qm, pq, pl.ctas_q, s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+    if (launch_bwd_kv(shape->d, setting, false, kv, pkv, pl.ctas_kv, s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+    return STREAMKL_OK;
 }
 
 streamkl_status streamkl_workspace_status(void* workspace, streamkl_stream_t stream, uint32_t* device_error) {

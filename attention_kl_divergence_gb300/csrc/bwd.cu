@@ -1,0 +1,713 @@
+// bwd.cu -- backward kernels of the attention KL divergence on sm_103a.
+//
+// Method: "StreamKL: Fast and Memory-Efficient KL Divergence for Boosting
+// Attention Distillation" (gist.science/paper/2606.20005, technical summary),
+// Methodology 2: the probabilities are regenerated tile by tile from the saved
+// log-sum-exps, P_t = exp(S_t - LSE_t), and the gradient of sum_i g_i KL_i is
+//   setting 1 (teacher fixed, student trainable): dS2 = g (P2 - P1)
+//   setting 2 (student fixed, teacher trainable): dS1 = g P1 ((S1-LSE1) - (S2-LSE2) - KL)
+// (the log-ratio taken from logit differences and the saved LSEs), followed by
+//   dQ_t = scale * dS K_t,   dK_t = scale * dS^T Q_t   for the trainable side t.
+//
+//   bwd_q_kernel   one 128-row query tile; loops over 64-key tiles; dQ in TMEM.
+//   bwd_kv_kernel  one 128-key tile; loops over 64-row query tiles; dK in TMEM.
+//                  FUSED also forms dQ^T = K_t^T dS^T per tile pair and adds it
+//                  to global dQ with atomics (each QK tile pair visited once).
+// The split mode runs both kernels (each recomputes the scores); the fused
+// mode runs bwd_kv_kernel<FUSED> alone after zeroing dQ.
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace streamkl {
+
+namespace {
+
+constexpr int kBwdTile = 64;  // the inner (streamed) tile of both backward kernels
+
+__device__ __noinline__ bool drain_wait_b(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t code) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, w, code));
+}
+
+// dS for one (query, key) pair from the raw dot products z1, z2.
+//   la = LSE1 * log2(e);  xb = LSE2 * log2(e) (setting 1) or LSE1 - LSE2 + KL (setting 2)
+template <int SETTING>
+__device__ __forceinline__ float dscore(float z1, float z2, float c, float scale, float la, float xb, float g) {
+    const float p1 = ex2(fmaf(z1, c, -la));
+    if (SETTING == 1) {
+        const float p2 = ex2(fmaf(z2, c, -xb));
+        return g * (p2 - p1);
+    } else {
+        return g * p1 * fmaf(scale, z1 - z2, -xb);
+    }
+}
+
+// Per-row constants of the recompute, for row `row` (flat into [B*H*Nq]).
+template <int SETTING>
+__device__ __forceinline__ void row_constants(const BwdParams& p, size_t row, bool valid, float& la, float& xb,
+                                              float& g) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    if (!valid) {
+        la = xb = g = 0.f;
+        return;
+    }
+    const float l1 = p.LSE1[row], l2 = p.LSE2[row];
+    la = l1 * kLog2e;
+    xb = SETTING == 1 ? l2 * kLog2e : (l1 - l2) + p.KL[row];
+    g = p.g[row];
+}
+
+// Write 32 dS values as two bf16 terms, hi = bf16(v) and lo = bf16(v - hi),
+// each as four 16-byte chunks of a 128-byte swizzled row of its own tile.
+// The gradient GEMMs consume hi and lo with the same other operand, so dS
+// enters them with ~16 significant bits instead of bf16's 8.
+__device__ __forceinline__ void store_ds_chunk(uint32_t tile_hi, uint32_t tile_lo, int row, int chunk0,
+                                               const float (&v)[32]) {
+    const uint32_t roff = row * 128;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float a = v[cc * 8 + 2 * k], b = v[cc * 8 + 2 * k + 1];
+            hi[k] = pack_bf16(a, b);
+            const float ha = __uint_as_float(hi[k] << 16), hb = __uint_as_float(hi[k] & 0xffff0000u);
+            lo[k] = pack_bf16(a - ha, b - hb);
+        }
+        const uint32_t off = roff + (((chunk0 + cc) ^ (row & 7)) << 4);
+        st_shared_v4(tile_hi + off, hi[0], hi[1], hi[2], hi[3]);
+        st_shared_v4(tile_lo + off, lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bwd_q: CTA = 128 query rows; 64-key tiles streamed through a 3-stage ring.
+// Warps: 0 TMA, 1 TMEM + MMA, 2-9 recompute/dS (two warpgroups, one query row
+// per thread, each taking 32 of the tile's 64 keys).
+// TMEM: S1|S2 double buffered (cols 0-255), dQ accumulator (cols 256-383).
+// ---------------------------------------------------------------------------
+template <int D, int NST>
+struct QSmem {
+    static constexpr int kQBytes = kBlockQ * D * 2;    // 128 rows
+    static constexpr int kKBytes = kBwdTile * D * 2;   // 64 rows
+    static constexpr int kDsBytes = kBlockQ * kBwdTile * 2;
+    static constexpr int q1 = 0;
+    static constexpr int q2 = kQBytes;
+    static constexpr int k = 2 * kQBytes;
+    static constexpr int kNumDs = 1;                  // dS buffers: the update computes before it stores
+    static constexpr int ds = k + 2 * NST * kKBytes;  // buffer b: hi at ds + 2*b*kDsBytes, lo right after
+    static constexpr int bars = ds + 2 * kNumDs * kDsBytes;
+    static constexpr int bar_q = bars;
+    static constexpr int bar_kfull = bar_q + 8;
+    static constexpr int bar_kempty = bar_kfull + 8 * NST;
+    static constexpr int bar_sfull = bar_kempty + 8 * NST;
+    static constexpr int bar_sempty = bar_sfull + 16;
+    static constexpr int bar_dsfull = bar_sempty + 16;
+    static constexpr int bar_dsempty = bar_dsfull + 16;
+    static constexpr int bar_done = bar_dsempty + 16;
+    static constexpr int misc = bar_done + 8;
+    static constexpr int total = misc + 16;
+    static constexpr int alloc = total + 1024;
+};
+
+template <int D, int NST, int SETTING>
+__global__ void __launch_bounds__(320, 1)
+    bwd_q_kernel(const __grid_constant__ CUtensorMap tQ1, const __grid_constant__ CUtensorMap tK1,
+                 const __grid_constant__ CUtensorMap tQ2, const __grid_constant__ CUtensorMap tK2,
+                 const BwdParams p) {
+    using L = QSmem<D, NST>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - smem_u32(smem_raw));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::misc + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::misc);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // head-major: resident CTAs share one head's key tiles through L2; causal:
+    // the heaviest (last) query tiles of a head first
+    const int bh = blockIdx.x / p.num_q_tiles;
+    const int qi = blockIdx.x - bh * p.num_q_tiles;
+    const int qt = p.causal ? (p.num_q_tiles - 1 - qi) : qi;
+    const int b = bh / p.H, h = bh - b * p.H;
+    const int q0 = qt * kBlockQ;
+    const int q_last = min(q0 + kBlockQ, p.Nq) - 1;
+    const int n_tiles = p.causal ? min(p.num_k_tiles, (q_last + p.diag_off) / kBwdTile + 1) : p.num_k_tiles;
+    // trainable side: setting 1 -> student (Q2, K2), setting 2 -> teacher (Q1, K1)
+    const uint32_t kt_off = SETTING == 1 ? L::kKBytes : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(base + L::bar_q, 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(base + L::bar_kfull + 8 * s, 1);
+            mbar_init(base + L::bar_kempty + 8 * s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(base + L::bar_sfull + 8 * s, 1);
+            mbar_init(base + L::bar_sempty + 8 * s, 256);
+            mbar_init(base + L::bar_dsfull + 8 * s, 256);
+            mbar_init(base + L::bar_dsempty + 8 * s, 1);
+        }
+        mbar_init(base + L::bar_done, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) tmem_alloc(base + L::misc, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{abort_flag, p.status, p.wait_ns};
+
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tensormap(&tQ1);
+            prefetch_tensormap(&tK1);
+            prefetch_tensormap(&tQ2);
+            prefetch_tensormap(&tK2);
+            const uint64_t keep = policy_evict_last();
+            mbar_arrive_expect_tx(base + L::bar_q, 2 * L::kQBytes);
+#pragma unroll
+            for (int c = 0; c < D / kSwizzleCols; ++c) {
+                tma_load_4d(base + L::q1 + c * kBlockQ * 128, &tQ1, base + L::bar_q, c * kSwizzleCols, q0, h, b);
+                tma_load_4d(base + L::q2 + c * kBlockQ * 128, &tQ2, base + L::bar_q, c * kSwizzleCols, q0, h, b);
+            }
+            int it = 0;
+            for (; it < n_tiles; ++it) {
+                const int s = it % NST;
+                if (!mbar_wait(base + L::bar_kempty + 8 * s, ((it / NST) & 1) ^ 1, wc, kErrWaitK)) break;
+                const uint32_t fb = base + L::bar_kfull + 8 * s;
+                mbar_arrive_expect_tx(fb, 2 * L::kKBytes);
+                const int k0 = it * kBwdTile;
+                const uint32_t k1s = base + L::k + 2 * s * L::kKBytes, k2s = k1s + L::kKBytes;
+#pragma unroll
+                for (int c = 0; c < D / kSwizzleCols; ++c) {
+                    tma_load_4d_hint(k1s + c * kBwdTile * 128, &tK1, fb, c * kSwizzleCols, k0, h, b, keep);
+                    tma_load_4d_hint(k2s + c * kBwdTile * 128, &tK2, fb, c * kSwizzleCols, k0, h, b, keep);
+                }
+            }
+            for (int j = max(0, it - NST); j < it; ++j) {
+                drain_wait_b(base + L::bar_kfull + 8 * (j % NST), (j / NST) & 1, p.wait_ns);
+                drain_wait_b(base + L::bar_kempty + 8 * (j % NST), (j / NST) & 1, p.wait_ns / 8 + 1000000);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc_bf16_f32(kBlockQ, kBwdTile);
+            constexpr uint32_t id_dq = idesc_bf16_f32(kBlockQ, D, 0, 1);
+            const uint32_t t_dq = tmem + 256;
+            int issued = 0;
+            auto issue_s = [&](int it) {
+                const int s = it % NST, buf = it & 1;
+                const uint32_t k1s = base + L::k + 2 * s * L::kKBytes;
+                const uint32_t d1 = tmem + buf * 128, d2 = d1 + 64;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qo = (kk >> 2) * kBlockQ * 128 + (kk & 3) * 32;
+                    const uint32_t ko = (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32;
+                    tc_mma_bf16(d1, smem_desc_k128(base + L::q1 + qo), smem_desc_k128(k1s + ko), id_s, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qo = (kk >> 2) * kBlockQ * 128 + (kk & 3) * 32;
+                    const uint32_t ko = (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32;
+                    tc_mma_bf16(d2, smem_desc_k128(base + L::q2 + qo), smem_desc_k128(k1s + L::kKBytes + ko), id_s,
+                                kk > 0);
+                }
+                tc_commit(base + L::bar_sfull + 8 * buf);
+            };
+            bool ok = mbar_wait(base + L::bar_q, 0, wc, kErrWaitQ) &&
+                      mbar_wait(base + L::bar_kfull, 0, wc, kErrWaitK);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                for (int it = 0; it < n_tiles; ++it) {
+                    if (it + 1 < n_tiles) {
+                        const int n1 = it + 1;
+                        if (!mbar_wait(base + L::bar_kfull + 8 * (n1 % NST), (n1 / NST) & 1, wc, kErrWaitK)) break;
+                        if (!mbar_wait(base + L::bar_sempty + 8 * (n1 & 1), ((n1 >> 1) & 1) ^ 1, wc, kErrWaitS))
+                            break;
+                        tc_fence_after();
+                        issue_s(n1);
+                    }
+                    const int s = it % NST, buf = it & 1;
+                    const int dsb = it % L::kNumDs;
+                    if (!mbar_wait(base + L::bar_dsfull + 8 * dsb, (it / L::kNumDs) & 1, wc, kErrWaitOther)) break;
+                    tc_fence_after();
+                    const uint32_t kts = base + L::k + 2 * s * L::kKBytes + kt_off;
+                    const uint32_t dss = base + L::ds + 2 * dsb * L::kDsBytes;
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)  // dS = hi + lo
+#pragma unroll
+                        for (int kk = 0; kk < kBwdTile / 16; ++kk)
+                            tc_mma_bf16(t_dq, smem_desc_k128(dss + part * L::kDsBytes + kk * 32),
+                                        smem_desc_mn128(kts + kk * 16 * 128, kBwdTile * 128), id_dq,
+                                        (it | kk | part) != 0);
+                    tc_commit(base + L::bar_dsempty + 8 * dsb);
+                    tc_commit(base + L::bar_kempty + 8 * s);
+                    ++issued;
+                }
+                if (issued == n_tiles) tc_commit(base + L::bar_done);
+            }
+            if (*abort_flag) drain_wait_b(base + L::bar_done, 0, p.wait_ns / 8 + 1000000);
+        }
+    } else {
+        // Two warpgroups: warps 2-5 take keys 0-31 of every tile, warps 6-9 keys 32-63.
+        const int wg = (warp - 2) >> 2;
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;
+        const int i = q0 + row;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const float c = p.scale_log2e;
+        const size_t grow = static_cast<size_t>(bh) * p.Nq + i;
+        float la, xb, g;
+        row_constants<SETTING>(p, grow, i < p.Nq, la, xb, g);
+        const int limit = p.causal ? min(i + p.diag_off, p.Nk - 1) : p.Nk - 1;
+        bool ok = true;
+        for (int it = 0; it < n_tiles; ++it) {
+            const int buf = it & 1;
+            if (!wait_all(base + L::bar_sfull + 8 * buf, (it >> 1) & 1, wc, kErrWaitS)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t t1 = tl + buf * 128 + wg * 32, t2 = t1 + 64;
+            const int dsb = it % L::kNumDs;
+            const uint32_t dss = base + L::ds + 2 * dsb * L::kDsBytes;
+            float z1[32], z2[32];
+            tmem_ld32(t1, z1);
+            tmem_ld32(t2, z2);
+            tc_wait_ld();
+            tc_fence_before();
+            mbar_arrive(base + L::bar_sempty + 8 * buf);
+            const int last = limit - (it * kBwdTile + wg * 32);
+            float v[32];
+            if (last >= 31) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = dscore<SETTING>(z1[e], z2[e], c, p.scale, la, xb, g);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    v[e] = dscore<SETTING>(z1[e], z2[e], c, p.scale, la, xb, g);
+                    if (e > last) v[e] = 0.f;
+                }
+            }
+            if (!wait_all(base + L::bar_dsempty + 8 * dsb, ((it / L::kNumDs) & 1) ^ 1, wc, kErrWaitOther)) {
+                ok = false;
+                break;
+            }
+            store_ds_chunk(dss, dss + L::kDsBytes, row, wg * 4, v);
+            fence_proxy_async_smem();
+            mbar_arrive(base + L::bar_dsfull + 8 * dsb);
+        }
+        // epilogue: dQ row = scale * accumulator; each warpgroup writes half the columns
+        if (ok && wait_all(base + L::bar_done, 0, wc, kErrWaitOther)) {
+            tc_fence_after();
+            float* out = p.dQ + grow * D;
+#pragma unroll 1
+            for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 32) {
+                float v[32];
+                tmem_ld32(tl + 256 + c0, v);
+                tc_wait_ld();
+                if (i < p.Nq) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(out + c0 + e) =
+                            make_float4(v[e] * p.scale, v[e + 1] * p.scale, v[e + 2] * p.scale, v[e + 3] * p.scale);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// bwd_kv: CTA = 128 keys; 64-row query tiles streamed through a 3-stage ring.
+// Warps: 0 TMA + per-row constants, 1 TMEM + MMA, 2-9 recompute/dS (two
+// warpgroups, one key per thread, each taking 32 of the tile's 64 query rows),
+// 10-13 (FUSED) dQ^T accumulator -> global atomics.
+// TMEM: S1^T|S2^T double buffered (cols 0-255), dK (256-383), dQ^T x2 (384-511).
+// ---------------------------------------------------------------------------
+template <int D, int NST>
+struct KvSmem {
+    static constexpr int kKBytes = kBlockK * D * 2;    // 128 keys
+    static constexpr int kQBytes = kBwdTile * D * 2;   // 64 query rows
+    static constexpr int kDsBytes = kBlockK * kBwdTile * 2;
+    static constexpr int k1 = 0;
+    static constexpr int k2 = kKBytes;
+    static constexpr int q = 2 * kKBytes;
+    static constexpr int kNumDs = 1;                   // dS buffers: the update computes before it stores
+    static constexpr int ds = q + 2 * NST * kQBytes;   // buffer b: hi at ds + 2*b*kDsBytes, lo right after
+    static constexpr int vec = ds + 2 * kNumDs * kDsBytes;  // [NST][3][64] floats
+    static constexpr int bars = vec + NST * 3 * kBwdTile * 4;
+    static constexpr int bar_k = bars;
+    static constexpr int bar_qfull = bar_k + 8;
+    static constexpr int bar_qempty = bar_qfull + 8 * NST;
+    static constexpr int bar_sfull = bar_qempty + 8 * NST;
+    static constexpr int bar_sempty = bar_sfull + 16;
+    static constexpr int bar_dsfull = bar_sempty + 16;
+    static constexpr int bar_dsempty = bar_dsfull + 16;
+    static constexpr int bar_dqfull = bar_dsempty + 16;
+    static constexpr int bar_dqempty = bar_dqfull + 16;
+    static constexpr int bar_done = bar_dqempty + 16;
+    static constexpr int misc = bar_done + 8;
+    static constexpr int total = misc + 16;
+    static constexpr int alloc = total + 1024;
+};
+
+template <int D, int NST, int SETTING, bool FUSED>
+__global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
+    bwd_kv_kernel(const __grid_constant__ CUtensorMap tQ1, const __grid_constant__ CUtensorMap tK1,
+                  const __grid_constant__ CUtensorMap tQ2, const __grid_constant__ CUtensorMap tK2,
+                  const BwdParams p) {
+    using L = KvSmem<D, NST>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - smem_u32(smem_raw));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::misc + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::misc);
+    float* vec = reinterpret_cast<float*>(gbase + L::vec);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // head-major: resident CTAs share one head's query tiles through L2; key
+    // tile 0 sees the most query rows under a causal mask and comes first
+    const int bh = blockIdx.x / p.num_k_tiles;
+    const int nt = blockIdx.x - bh * p.num_k_tiles;
+    const int b = bh / p.H, h = bh - b * p.H;
+    const int n0 = nt * kBlockK;
+    // first 64-row query tile with a row that sees key n0 (row i sees keys j <= i + diag_off)
+    const int m_start = p.causal ? max(0, (n0 - p.diag_off) / kBwdTile) : 0;
+    const int n_tiles = p.num_q_tiles - m_start;
+    const uint32_t kt_tile = base + (SETTING == 1 ? L::k2 : L::k1);  // trainable keys
+    const uint32_t qt_off = SETTING == 1 ? L::kQBytes : 0;           // trainable queries within a stage
+
+    if (threadIdx.x == 0) {
+        mbar_init(base + L::bar_k, 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(base + L::bar_qfull + 8 * s, 33);
+            mbar_init(base + L::bar_qempty + 8 * s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(base + L::bar_sfull + 8 * s, 1);
+            mbar_init(base + L::bar_sempty + 8 * s, 256);
+            mbar_init(base + L::bar_dsfull + 8 * s, 256);
+            mbar_init(base + L::bar_dsempty + 8 * s, 1);
+            mbar_init(base + L::bar_dqfull + 8 * s, 1);
+            mbar_init(base + L::bar_dqempty + 8 * s, 128);
+        }
+        mbar_init(base + L::bar_done, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) tmem_alloc(base + L::misc, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx wc{abort_flag, p.status, p.wait_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA + row constants
+        if (lane == 0) {
+            prefetch_tensormap(&tQ1);
+            prefetch_tensormap(&tK1);
+            prefetch_tensormap(&tQ2);
+            prefetch_tensormap(&tK2);
+            mbar_arrive_expect_tx(base + L::bar_k, 2 * L::kKBytes);
+#pragma unroll
+            for (int c = 0; c < D / kSwizzleCols; ++c) {
+                tma_load_4d(base + L::k1 + c * kBlockK * 128, &tK1, base + L::bar_k, c * kSwizzleCols, n0, h, b);
+                tma_load_4d(base + L::k2 + c * kBlockK * 128, &tK2, base + L::bar_k, c * kSwizzleCols, n0, h, b);
+            }
+        }
+        const uint64_t keep = policy_evict_last();
+        int m = 0;
+        for (; m < n_tiles; ++m) {
+            const int s = m % NST;
+            if (!wait_all(base + L::bar_qempty + 8 * s, ((m / NST) & 1) ^ 1, wc, kErrWaitOther)) break;
+            const int r0 = (m_start + m) * kBwdTile;
+            const uint32_t fb = base + L::bar_qfull + 8 * s;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(fb, 2 * L::kQBytes);
+                const uint32_t q1s = base + L::q + 2 * s * L::kQBytes, q2s = q1s + L::kQBytes;
+#pragma unroll
+                for (int c = 0; c < D / kSwizzleCols; ++c) {
+                    tma_load_4d_hint(q1s + c * kBwdTile * 128, &tQ1, fb, c * kSwizzleCols, r0, h, b, keep);
+                    tma_load_4d_hint(q2s + c * kBwdTile * 128, &tQ2, fb, c * kSwizzleCols, r0, h, b, keep);
+                }
+            }
+            float* v = vec + s * 3 * kBwdTile;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int r = lane + 32 * k;
+                const int i = r0 + r;
+                float la, xb, g;
+                row_constants<SETTING>(p, static_cast<size_t>(bh) * p.Nq + i, i < p.Nq, la, xb, g);
+                v[r] = la;
+                v[kBwdTile + r] = xb;
+                v[2 * kBwdTile + r] = g;
+            }
+            mbar_arrive(fb);
+        }
+        if (lane == 0) {
+            for (int j = max(0, m - NST); j < m; ++j) {
+                drain_wait_b(base + L::bar_qfull + 8 * (j % NST), (j / NST) & 1, p.wait_ns);
+                drain_wait_b(base + L::bar_qempty + 8 * (j % NST), (j / NST) & 1, p.wait_ns / 8 + 1000000);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA
+        if (lane == 0) {
+            constexpr uint32_t id_s = idesc_bf16_f32(kBlockK, kBwdTile);
+            constexpr uint32_t id_dk = idesc_bf16_f32(kBlockK, D, 0, 1);
+            constexpr uint32_t id_dq = idesc_bf16_f32(D, kBwdTile, 1, 1);
+            const uint32_t t_dk = tmem + 256;
+            auto issue_s = [&](int m) {
+                const int s = m % NST, buf = m & 1;
+                const uint32_t q1s = base + L::q + 2 * s * L::kQBytes;
+                const uint32_t d1 = tmem + buf * 128, d2 = d1 + 64;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t ko = (kk >> 2) * kBlockK * 128 + (kk & 3) * 32;
+                    const uint32_t qo = (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32;
+                    tc_mma_bf16(d1, smem_desc_k128(base + L::k1 + ko), smem_desc_k128(q1s + qo), id_s, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t ko = (kk >> 2) * kBlockK * 128 + (kk & 3) * 32;
+                    const uint32_t qo = (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32;
+                    tc_mma_bf16(d2, smem_desc_k128(base + L::k2 + ko), smem_desc_k128(q1s + L::kQBytes + qo), id_s,
+                                kk > 0);
+                }
+                tc_commit(base + L::bar_sfull + 8 * buf);
+            };
+            int issued = 0;
+            bool ok = mbar_wait(base + L::bar_k, 0, wc, kErrWaitK) &&
+                      mbar_wait(base + L::bar_qfull, 0, wc, kErrWaitQ);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                for (int m = 0; m < n_tiles; ++m) {
+                    if (m + 1 < n_tiles) {
+                        const int n1 = m + 1;
+                        if (!mbar_wait(base + L::bar_qfull + 8 * (n1 % NST), (n1 / NST) & 1, wc, kErrWaitQ)) break;
+                        if (!mbar_wait(base + L::bar_sempty + 8 * (n1 & 1), ((n1 >> 1) & 1) ^ 1, wc, kErrWaitS))
+                            break;
+                        tc_fence_after();
+                        issue_s(n1);
+                    }
+                    const int s = m % NST, buf = m & 1;
+                    const int dsb = m % L::kNumDs;
+                    if (!mbar_wait(base + L::bar_dsfull + 8 * dsb, (m / L::kNumDs) & 1, wc, kErrWaitOther)) break;
+                    tc_fence_after();
+                    const uint32_t dss = base + L::ds + 2 * dsb * L::kDsBytes;
+                    const uint32_t qts = base + L::q + 2 * s * L::kQBytes + qt_off;
+                    // dK += dS^T Q_t : A = dS^T (K-major over queries), B = Q_t (MN-major); dS = hi + lo
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int kk = 0; kk < kBwdTile / 16; ++kk)
+                            tc_mma_bf16(t_dk, smem_desc_k128(dss + part * L::kDsBytes + kk * 32),
+                                        smem_desc_mn128(qts + kk * 16 * 128, kBwdTile * 128), id_dk,
+                                        (m | kk | part) != 0);
+                    if (FUSED) {
+                        // dQ^T = K_t^T dS^T : A = K_t (MN-major), B = dS^T (MN-major), K = 128 keys
+                        if (!mbar_wait(base + L::bar_dqempty + 8 * buf, ((m >> 1) & 1) ^ 1, wc, kErrWaitOther)) break;
+                        tc_fence_after();
+                        const uint32_t t_dq = tmem + 384 + buf * kBwdTile;
+#pragma unroll
+                        for (int part = 0; part < 2; ++part)
+#pragma unroll
+                            for (int kk = 0; kk < kBlockK / 16; ++kk)
+                                tc_mma_bf16(t_dq, smem_desc_mn128(kt_tile + kk * 16 * 128, kBlockK * 128),
+                                            smem_desc_mn128(dss + part * L::kDsBytes + kk * 16 * 128, kBlockK * 128),
+                                            id_dq, (kk | part) != 0);
+                        tc_commit(base + L::bar_dqfull + 8 * buf);
+                    }
+                    tc_commit(base + L::bar_dsempty + 8 * dsb);
+                    tc_commit(base + L::bar_qempty + 8 * s);
+                    ++issued;
+                }
+                if (issued == n_tiles) tc_commit(base + L::bar_done);
+            }
+            if (*abort_flag) drain_wait_b(base + L::bar_done, 0, p.wait_ns / 8 + 1000000);
+        }
+    } else if (warp < 10) {
+        // ------------------------------------------------ recompute + dS^T
+        // Two warpgroups: warps 2-5 take query rows 0-31 of every tile, warps
+        // 6-9 rows 32-63; one key per thread.
+        const int wg = (warp - 2) >> 2;
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;
+        const int j = n0 + row;  // key index
+        const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const float c = p.scale_log2e;
+        const bool key_ok = j < p.Nk;
+        bool ok = true;
+        for (int m = 0; m < n_tiles; ++m) {
+            const int s = m % NST, buf = m & 1;
+            if (!wait_all(base + L::bar_sfull + 8 * buf, (m >> 1) & 1, wc, kErrWaitS) ||
+                !wait_all(base + L::bar_qfull + 8 * s, (m / NST) & 1, wc, kErrWaitQ)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int r0 = (m_start + m) * kBwdTile + wg * 32;  // first query row of this chunk
+            const uint32_t t1 = tl + buf * 128 + wg * 32, t2 = t1 + 64;
+            const int dsb = m % L::kNumDs;
+            const uint32_t dss = base + L::ds + 2 * dsb * L::kDsBytes;
+            float z1[32], z2[32];
+            tmem_ld32(t1, z1);
+            tmem_ld32(t2, z2);
+            tc_wait_ld();
+            tc_fence_before();
+            mbar_arrive(base + L::bar_sempty + 8 * buf);
+            // per-query constants of this chunk: 128-bit broadcast loads
+            const float4* v4 = reinterpret_cast<const float4*>(vec + s * 3 * kBwdTile + wg * 32);
+            float dsv[32];
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+                const float4 a = v4[e4], x = v4[kBwdTile / 4 + e4], gg = v4[kBwdTile / 2 + e4];
+                const float la[4] = {a.x, a.y, a.z, a.w}, xb[4] = {x.x, x.y, x.z, x.w},
+                            gv[4] = {gg.x, gg.y, gg.z, gg.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int e = 4 * e4 + k;
+                    dsv[e] = dscore<SETTING>(z1[e], z2[e], c, p.scale, la[k], xb[k], gv[k]);
+                }
+            }
+            // query i = r0 + e sees key j iff j <= i + diag_off; keys past Nk contribute nothing
+            const int first = p.causal ? (j - p.diag_off) - r0 : -1;
+            if (first > 0 || !key_ok) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (e < first || !key_ok) dsv[e] = 0.f;
+            }
+            if (!wait_all(base + L::bar_dsempty + 8 * dsb, ((m / L::kNumDs) & 1) ^ 1, wc, kErrWaitOther)) {
+                ok = false;
+                break;
+            }
+            store_ds_chunk(dss, dss + L::kDsBytes, row, wg * 4, dsv);
+            fence_proxy_async_smem();
+            mbar_arrive(base + L::bar_dsfull + 8 * dsb);
+        }
+        // epilogue: dK row = scale * accumulator; each warpgroup writes half the columns
+        if (ok && wait_all(base + L::bar_done, 0, wc, kErrWaitOther)) {
+            tc_fence_after();
+            float* out = p.dK + (static_cast<size_t>(bh) * p.Nk + j) * D;
+#pragma unroll 1
+            for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 32) {
+                float v[32];
+                tmem_ld32(tl + 256 + c0, v);
+                tc_wait_ld();
+                if (key_ok) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4*>(out + c0 + e) =
+                            make_float4(v[e] * p.scale, v[e + 1] * p.scale, v[e + 2] * p.scale, v[e + 3] * p.scale);
+                }
+            }
+        }
+    } else if (FUSED) {
+        // ------------------------------------------------ dQ^T -> atomics into dQ
+        const int wq = warp & 3;
+        const int f = wq * 32 + lane;  // feature = TMEM lane
+        const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        for (int m = 0; m < n_tiles; ++m) {
+            const int buf = m & 1;
+            if (!wait_all(base + L::bar_dqfull + 8 * buf, (m >> 1) & 1, wc, kErrWaitOther)) break;
+            tc_fence_after();
+            float v0[32], v1[32];
+            tmem_ld32(tl + 384 + buf * kBwdTile, v0);
+            tmem_ld32(tl + 384 + buf * kBwdTile + 32, v1);
+            tc_wait_ld();
+            tc_fence_before();
+            mbar_arrive(base + L::bar_dqempty + 8 * buf);
+            const int r0 = (m_start + m) * kBwdTile;
+            float* out = p.dQ + (static_cast<size_t>(bh) * p.Nq + r0) * D + f;
+            const int nrow = min(kBwdTile, p.Nq - r0);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                if (e < nrow) red_add_f32(out + static_cast<size_t>(e) * D, v0[e] * p.scale);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                if (e + 32 < nrow) red_add_f32(out + static_cast<size_t>(e + 32) * D, v1[e] * p.scale);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int D, int SETTING>
+cudaError_t launch_q_impl(const CUtensorMap* maps, const BwdParams& p, int ctas, cudaStream_t st) {
+    constexpr int NST = D == 128 ? 4 : 6;
+    static_assert(QSmem<D, NST>::alloc <= 232448, "shared memory");
+    auto k = bwd_q_kernel<D, NST, SETTING>;
+    cudaError_t e = set_smem(k, QSmem<D, NST>::alloc);
+    if (e != cudaSuccess) return e;
+    k<<<ctas, 320, QSmem<D, NST>::alloc, st>>>(maps[0], maps[1], maps[2], maps[3], p);
+    return cudaGetLastError();
+}
+
+template <int D, int SETTING, bool FUSED>
+cudaError_t launch_kv_impl(const CUtensorMap* maps, const BwdParams& p, int ctas, cudaStream_t st) {
+    constexpr int NST = D == 128 ? 3 : 6;
+    static_assert(KvSmem<D, NST>::alloc <= 232448, "shared memory");
+    auto k = bwd_kv_kernel<D, NST, SETTING, FUSED>;
+    cudaError_t e = set_smem(k, KvSmem<D, NST>::alloc);
+    if (e != cudaSuccess) return e;
+    k<<<ctas, FUSED ? 448 : 320, KvSmem<D, NST>::alloc, st>>>(maps[0], maps[1], maps[2], maps[3], p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_q(int d, int setting, const CUtensorMap* maps, const BwdParams& p, int ctas,
+                         cudaStream_t stream) {
+    if (d == 128) return setting == 1 ? launch_q_impl<128, 1>(maps, p, ctas, stream)
+                                      : launch_q_impl<128, 2>(maps, p, ctas, stream);
+    return setting == 1 ? launch_q_impl<64, 1>(maps, p, ctas, stream) : launch_q_impl<64, 2>(maps, p, ctas, stream);
+}
+
+cudaError_t launch_bwd_kv(int d, int setting, bool fused, const CUtensorMap* maps, const BwdParams& p, int ctas,
+                          cudaStream_t stream) {
+    if (d == 128) {
+        if (fused)
+            return setting == 1 ? launch_kv_impl<128, 1, true>(maps, p, ctas, stream)
+                                : launch_kv_impl<128, 2, true>(maps, p, ctas, stream);
+        return setting == 1 ? launch_kv_impl<128, 1, false>(maps, p, ctas, stream)
+                            : launch_kv_impl<128, 2, false>(maps, p, ctas, stream);
+    }
+    if (fused) return cudaErrorInvalidValue;  // the fused dQ^T MMA needs M = d = 128
+    return setting == 1 ? launch_kv_impl<64, 1, false>(maps, p, ctas, stream)
+                        : launch_kv_impl<64, 2, false>(maps, p, ctas, stream);
+}
+
+}  // namespace streamkl

@@ -39,6 +39,25 @@ struct FwdParams {
     unsigned long long wait_ns;
 };
 
+// Backward (both kernels).  Tile counts are in the kernel's own tile units.
+struct BwdParams {
+    int B, H, Nq, Nk;
+    int num_q_tiles;     // bwd_q: 128-row tiles; bwd_kv: 64-row tiles
+    int num_k_tiles;     // bwd_q: 64-key tiles;  bwd_kv: 128-key tiles
+    int causal;
+    int diag_off;        // Nk - Nq
+    float scale;
+    float scale_log2e;
+    const float* g;      // [B*H*Nq] upstream gradient dL/dKL
+    const float* KL;
+    const float* LSE1;
+    const float* LSE2;
+    float* dQ;           // [B*H*Nq, d]
+    float* dK;           // [B*H*Nk, d]
+    unsigned int* status;
+    unsigned long long wait_ns;
+};
+
 // Combine of Split-K partial states.
 struct CombineParams {
     int rows;            // B*H*Nq

@@ -40,7 +40,8 @@ struct TileSmem {
     static constexpr int bar_sfull = bar_kempty + 8 * NST;
     static constexpr int bar_sempty = bar_sfull + 16;
     static constexpr int misc = bar_sempty + 16;  // tmem base (4 B), abort flag (4 B)
-    static constexpr int total = misc + 16;
+    static constexpr int red = misc + 16;         // [5][128] floats: second warpgroup's row states
+    static constexpr int total = red + 5 * 128 * 4;
     static constexpr int alloc = total + 1024;    // slack for 1024-byte alignment
 };
 
@@ -121,12 +122,13 @@ __device__ __forceinline__ void store_row(const FwdParams& p, size_t row, int sp
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Tile forward.  CTA = 6 warps: warp 0 issues TMA, warp 1 owns TMEM and issues
-// the MMAs, warps 2-5 (one per TMEM lane quarter) run the online update, one
-// query row per thread.  TMEM: two buffers x (S1 | S2), 128 columns each.
+// Tile forward.  CTA = 10 warps: warp 0 issues TMA, warp 1 owns TMEM and
+// issues the MMAs, warps 2-9 run the online update (two warpgroups, one query
+// row per thread each, splitting the tile's columns).  TMEM: two buffers x
+// (S1 | S2), 128 columns each.
 // ---------------------------------------------------------------------------
 template <int D, int NST>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     fwd_tile_kernel(const __grid_constant__ CUtensorMap tQ1, const __grid_constant__ CUtensorMap tK1,
                     const __grid_constant__ CUtensorMap tQ2, const __grid_constant__ CUtensorMap tK2,
                     const FwdParams p) {
@@ -139,13 +141,14 @@ __global__ void __launch_bounds__(192, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // ---- which (query tile, head, split) this CTA owns; causal: heaviest first
-    const int BH = p.B * p.H;
-    const int per_q = BH * p.num_splits;
-    const int qi = blockIdx.x / per_q;
-    const int rem = blockIdx.x - qi * per_q;
-    const int bh = rem / p.num_splits;
-    const int split = rem - bh * p.num_splits;
+    // ---- which (head, query tile, split) this CTA owns.  Head-major order:
+    // the CTAs resident at one time share one head's key tiles through L2.
+    // Causal: the heaviest (last) query tiles of a head come first.
+    const int per_head = p.num_q_tiles * p.num_splits;
+    const int bh = blockIdx.x / per_head;
+    const int rem = blockIdx.x - bh * per_head;
+    const int qi = rem / p.num_splits;
+    const int split = rem - qi * p.num_splits;
     const int qt = p.causal ? (p.num_q_tiles - 1 - qi) : qi;
     const int b = bh / p.H, h = bh - b * p.H;
     const int q0 = qt * kBlockQ;
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(base + L::bar_sfull + 8 * s, 1);
-            mbar_init(base + L::bar_sempty + 8 * s, 128);
+            mbar_init(base + L::bar_sempty + 8 * s, 256);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -248,6 +251,11 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         // ------------------------------------------------------------ online update
+        // Two warpgroups: warps 2-5 take columns 0-63 of every tile, warps 6-9
+        // columns 64-127, each with its own running state for its columns;
+        // the two states of a row are merged at the end (the same log-sum-exp
+        // merge as the Split-K combine).
+        const int wg = (warp - 2) >> 2;
         const int wq = warp & 3;
         const int row = wq * 32 + lane;
         const int i = q0 + row;
@@ -267,12 +275,13 @@ __global__ void __launch_bounds__(192, 1)
             const int jrem = limit - (kt_begin + it) * kBlockK;  // last visible column of this tile
             const uint32_t t1 = tl + buf * 2 * kBlockK, t2 = t1 + kBlockK;
 #pragma unroll 1
-            for (int ch = 0; ch < kBlockK / 32; ++ch) {
+            for (int cc = 0; cc < 2; ++cc) {
+                const int ch = 2 * wg + cc;
                 float z1[32], z2[32];
                 tmem_ld32(t1 + ch * 32, z1);
                 tmem_ld32(t2 + ch * 32, z2);
                 tc_wait_ld();
-                if (ch == kBlockK / 32 - 1) {
+                if (cc == 1) {
                     tc_fence_before();
                     mbar_arrive(base + L::bar_sempty + 8 * buf);
                 }
@@ -283,7 +292,20 @@ __global__ void __launch_bounds__(192, 1)
                     update_chunk<true>(z1, z2, last, st, c, tau);
             }
         }
-        if (i < p.Nq) store_row(p, static_cast<size_t>(bh) * p.Nq + i, split, st, !ok || *abort_flag);
+        float* red = reinterpret_cast<float*>(gbase + L::red);
+        if (wg == 1) {
+            red[row] = st.m1;
+            red[128 + row] = st.l1;
+            red[256 + row] = st.acc;
+            red[384 + row] = st.m2;
+            red[512 + row] = st.l2;
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight update warps only
+        if (wg == 0) {
+            const RowState o{red[row], red[128 + row], red[256 + row], red[384 + row], red[512 + row]};
+            merge_state(st, o, c);
+            if (i < p.Nq) store_row(p, static_cast<size_t>(bh) * p.Nq + i, split, st, !ok || *abort_flag);
+        }
     }
 
     tc_fence_before();
@@ -559,12 +581,12 @@ cudaError_t launch_fwd_tile(int d, const CUtensorMap* maps, const FwdParams& p, 
         constexpr int NST = 2;
         auto k = fwd_tile_kernel<128, NST>;
         if ((e = ensure_smem(k, TileSmem<128, NST>::alloc)) != cudaSuccess) return e;
-        k<<<ctas, 192, TileSmem<128, NST>::alloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+        k<<<ctas, 320, TileSmem<128, NST>::alloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
     } else {
         constexpr int NST = 4;
         auto k = fwd_tile_kernel<64, NST>;
         if ((e = ensure_smem(k, TileSmem<64, NST>::alloc)) != cudaSuccess) return e;
-        k<<<ctas, 192, TileSmem<64, NST>::alloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+        k<<<ctas, 320, TileSmem<64, NST>::alloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
     }
     return cudaGetLastError();
 }

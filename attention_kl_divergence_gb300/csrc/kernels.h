@@ -14,4 +14,11 @@ cudaError_t launch_fwd_decode(int d, const CUtensorMap* maps, const FwdParams& p
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 int fwd_tile_stages(int d);
 
+// Backward.  bwd_q maps: Q boxes of 128 rows, K boxes of 64 rows; bwd_kv maps:
+// Q boxes of 64 rows, K boxes of 128 rows.
+cudaError_t launch_bwd_q(int d, int setting, const CUtensorMap* maps, const BwdParams& p, int ctas,
+                         cudaStream_t stream);
+cudaError_t launch_bwd_kv(int d, int setting, bool fused, const CUtensorMap* maps, const BwdParams& p, int ctas,
+                          cudaStream_t stream);
+
 }  // namespace streamkl

@@ -61,7 +61,7 @@ struct WaitCtx {
     uint64_t limit_ns;
 };
 
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t code) {
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t code) {
     uint64_t t0 = global_timer_ns();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -203,13 +203,47 @@ __device__ __forceinline__ uint64_t smem_desc_k128(uint32_t saddr) {
     return desc;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Shared-memory matrix descriptor for an MN-major operand stored as 128-byte
+// swizzled rows along K: each row holds 64 consecutive M (or N) elements,
+// 8-row groups along K are 1024 bytes apart and consecutive 64-element atoms
+// along M/N are `atom_stride` bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t saddr, uint32_t atom_stride) {
+    uint64_t desc = 0;
+    desc |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);          // start address
+    desc |= static_cast<uint64_t>((atom_stride >> 4) & 0x3FFFu) << 16;  // leading byte offset: MN atoms
+    desc |= static_cast<uint64_t>(1024u >> 4) << 32;                // stride byte offset: 8 K-rows
+    desc |= static_cast<uint64_t>(1u) << 46;                        // descriptor version (tcgen05)
+    desc |= static_cast<uint64_t>(2u) << 61;                        // swizzle mode: 128 B
+    return desc;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D.  a_mn / b_mn mark
+// an operand stored MN-major (transposed) instead of K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn = 0, int b_mn = 0) {
     return (1u << 4)                                  // D format: f32
            | (1u << 7)                                // A format: bf16
            | (1u << 10)                               // B format: bf16
+           | (static_cast<uint32_t>(a_mn & 1) << 15)  // A major-ness
+           | (static_cast<uint32_t>(b_mn & 1) << 16)  // B major-ness
            | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Store four 32-bit words (16 bytes) to shared memory.
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// Pack two floats to bf16x2 (round to nearest even); `lo` lands in the low half.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
 // ---------------------------------------------------------------------------

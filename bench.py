@@ -1,0 +1,373 @@
+"""Benchmark of the fused attention KL divergence (libstreamkl) on GB300.
+
+One step = the whole hot path on one batch: forward (KL, LSE1, LSE2) plus the
+recompute backward in both settings (setting 1: gradients to the student
+Q2/K2; setting 2: gradients to the teacher Q1/K1), on B=1, H=32,
+N_Q=N_K=65536, d=128, bf16, causal -- the workload the headline metric is
+quoted on.  Inputs are seeded synthetic tensors (teacher ~ N(0,1), student =
+teacher + 0.3 N(0,1)), resident in HBM; at 2 GiB they exceed the 129 MB L2.
+
+Printed (rank 0, one JSON line): the metric in TFLOP/s of algorithmic work
+(forward 4 d per visible pair, each backward 8 d per visible pair), ms per
+step and per pass, the roofline of the dominant kernel, the end-to-end rate
+through the C ABI with host buffers, clocks, and the float64 CPU oracle timed
+on a bounded sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun every rank runs its own copy of the workload (heads are
+independent, no collective on the data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from attention_kl_divergence_gb300 import WORKLOADS, make_g, make_workload  # noqa: E402
+
+WORKLOAD = "64k_causal"
+METRIC = "fwd/bwd TFLOP/s and ms at 64K causal, fraction of GB300 BF16 tensor peak"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"streamkl_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.out,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[2] > 300.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in loaded for k, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(loaded), "reasons": reasons}
+
+
+def gpu_id(dev):
+    """nvidia-smi id of a torch device (its UUID, robust to CUDA_VISIBLE_DEVICES)."""
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev.index or 0)
+
+
+def flush_l2(buf):
+    buf.add_(1)  # a write larger than L2 between timed steps
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg (the float64 oracle as it stands, bounded sample)
+# ---------------------------------------------------------------------------
+
+def cpu_oracle_sample(w, budget_s=15.0):
+    """Time the oracle's forward and both settings' dQ on sampled query rows of
+    one head of the workload (each row sees up to 64K keys).  Rate in TFLOP/s
+    of the same algorithmic work the GPU metric counts per pair."""
+    from oracle import oracle
+    from attention_kl_divergence_gb300 import make_qk
+    g = make_g(1, 1, w.Nq, w.g_value)
+    Q1, K1, Q2, K2 = make_qk(1, 1, w.Nq, w.Nk, w.d, w.sigma, w.teacher_scale, w.seed, device="cpu")
+    rng = np.random.default_rng(0)
+    cores = oracle.max_threads()
+    n = cores * 2
+    done_pairs, elapsed, nrows = 0, 0.0, 0
+    Q1n, K1n, Q2n, K2n = (oracle._f64(t) for t in (Q1, K1, Q2, K2))
+    gn = oracle._f64(g)
+    while elapsed < budget_s and nrows < 4096:
+        rows = rng.integers(0, w.Nq, size=n)
+        t0 = time.perf_counter()
+        oracle.fwd_rows(Q1n, K1n, Q2n, K2n, rows, causal=w.causal)
+        oracle.bwd_dq_rows(1, gn, Q1n, K1n, Q2n, K2n, rows, causal=w.causal)
+        oracle.bwd_dq_rows(2, gn, Q1n, K1n, Q2n, K2n, rows, causal=w.causal)
+        elapsed += time.perf_counter() - t0
+        off = w.Nk - w.Nq
+        done_pairs += int(sum(min(w.Nk, int(i) + off + 1) if w.causal else w.Nk for i in rows))
+        nrows += n
+    # algorithmic flops the GPU metric credits for these pairs: 4d (fwd) + 2 x 8d (bwd)
+    flops = 20 * w.d * done_pairs
+    return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{nrows} random query rows of one head of {w.name} (N_Q={w.Nq} N_K={w.Nk} d={w.d}): "
+                      f"forward + dQ of both settings per row, {elapsed:.1f} s, float64, "
+                      f"{done_pairs} visible pairs; credited 20*d flops per pair",
+            "seconds": elapsed}
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+
+def run_gpu(args):
+    from attention_kl_divergence_gb300 import streamkl
+
+    ws_, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(ws_, "nccl")
+    w = WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+    Q1, K1, Q2, K2 = make_workload(w, device=dev)
+    g = make_g(w.B, w.H, w.Nq, w.g_value, device=dev)
+    B, H, Nq, Nk, d = w.B, w.H, w.Nq, w.Nk, w.d
+    f32 = dict(dtype=torch.float32, device=dev)
+    KL, L1, L2 = (torch.empty((B, H, Nq), **f32) for _ in range(3))
+    dQ, dK = torch.empty((B, H, Nq, d), **f32), torch.empty((B, H, Nk, d), **f32)
+    fplan = streamkl.fwd_plan(Q1, K1, causal=w.causal)
+    bplan1 = streamkl.bwd_plan(Q1, K1, 1, causal=w.causal)
+    bplan2 = streamkl.bwd_plan(Q1, K1, 2, causal=w.causal)
+    wsp = streamkl.new_workspace(max(fplan.workspace_bytes, bplan1.workspace_bytes, bplan2.workspace_bytes), dev)
+    l2_flush = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        streamkl.kl_fwd(Q1, K1, Q2, K2, causal=w.causal, workspace=wsp, out=(KL, L1, L2))
+
+    def bwd(setting):
+        streamkl.kl_bwd(setting, g, Q1, K1, Q2, K2, KL, L1, L2, causal=w.causal, workspace=wsp, out=(dQ, dK))
+
+    launches_per_step = fplan.launches + bplan1.launches + bplan2.launches
+    if bplan1.path == streamkl.PATH_BWD_FUSED:
+        launches_per_step -= 1  # the dQ zero-fill is a memset, not one of our kernels
+    if bplan2.path == streamkl.PATH_BWD_FUSED:
+        launches_per_step -= 1
+
+    for _ in range(args.warmup):
+        fwd(), bwd(1), bwd(2)
+    torch.cuda.synchronize()
+    if streamkl.workspace_status(wsp):
+        raise RuntimeError("device error word set during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(ws_)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id(dev)) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for k in range(args.steps):
+            flush_l2(l2_flush)
+            e = ev[k]
+            e[0].record(stream)
+            fwd()
+            e[1].record(stream)
+            bwd(1)
+            e[2].record(stream)
+            bwd(2)
+            e[3].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws_)
+    status = streamkl.workspace_status(wsp)
+    fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    b1_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    b2_ms = statistics.median(e[2].elapsed_time(e[3]) for e in ev)
+    step_ms = sum(e[0].elapsed_time(e[3]) for e in ev) / args.steps
+    step_ms = max_over_ranks(step_ms, ws_, dev)
+
+    pairs = w.visible_pairs() * B * H
+    f_fwd, f_bwd = 4 * d * pairs, 8 * d * pairs
+    step_flops = f_fwd + 2 * f_bwd
+    value = step_flops * ws_ / (step_ms * 1e-3) / 1e12
+    peak_tf = peaks["bf16_tflops"]
+    kernels = {
+        "fwd": {"ms": fwd_ms, "tflops": f_fwd / fwd_ms / 1e9, "frac_bf16_peak": f_fwd / fwd_ms / 1e9 / peak_tf,
+                "path": "tile" if fplan.path == 0 else "decode", "splits": fplan.num_splits},
+        "bwd_setting1": {"ms": b1_ms, "tflops": f_bwd / b1_ms / 1e9, "frac_bf16_peak": f_bwd / b1_ms / 1e9 / peak_tf,
+                         "mode": "fused" if bplan1.path == streamkl.PATH_BWD_FUSED else "split"},
+        "bwd_setting2": {"ms": b2_ms, "tflops": f_bwd / b2_ms / 1e9, "frac_bf16_peak": f_bwd / b2_ms / 1e9 / peak_tf,
+                         "mode": "fused" if bplan2.path == streamkl.PATH_BWD_FUSED else "split"},
+    }
+    # Dominant single-launch kernel timed live: the forward tile kernel (one
+    # launch per forward call at this size); algorithmic 4*d flops per visible pair.
+    roofline = {"kernel": "fwd_tile_kernel", "bound": "tensor", "achieved": f_fwd / fwd_ms / 1e9, "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": f_fwd / fwd_ms / 1e9 / peak_tf, "traffic": None,
+                "peak_source": f"bf16_tflops ({peak_src}, burst)"}
+
+    # ---------------- end to end through the C ABI with host buffers
+    pin = dict(pin_memory=True)
+    hQ1, hK1, hQ2, hK2 = (t.cpu().pin_memory() for t in (Q1, K1, Q2, K2))
+    hg = g.cpu().pin_memory()
+    hKL = torch.empty((B, H, Nq), dtype=torch.float32, **pin)
+    h2d = sum(t.numel() * t.element_size() for t in (hQ1, hK1, hQ2, hK2, hg))
+    d2h = hKL.numel() * 4
+
+    def e2e_step():
+        Q1.copy_(hQ1, non_blocking=True), K1.copy_(hK1, non_blocking=True)
+        Q2.copy_(hQ2, non_blocking=True), K2.copy_(hK2, non_blocking=True)
+        g.copy_(hg, non_blocking=True)
+        fwd(), bwd(1), bwd(2)
+        hKL.copy_(KL, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws_)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, ws_, dev)
+    e2e = {"value": step_flops * ws_ / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    kl_mean = float(hKL.double().mean())
+
+    out = None
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws_, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) teacher, student +0.3 N(0,1))",
+            "config": {"workload": f"{w.name}: B={B} H={H} N_Q={Nq} N_K={Nk} d={d} "
+                                   f"{'causal' if w.causal else 'non-causal'}, fwd + bwd setting 1 + "
+                                   f"bwd setting 2 per step", "l2": "256 MB write between steps",
+                       "parallelism": f"heads-independent replicas x{ws_}"},
+            "kernels": kernels, "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "device_error_word": status, "kl_mean": kl_mean,
+            "peaks": {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"], "source": peak_src},
+        }
+        out["clocks"] = clk.summary()
+    return out, w
+
+
+def run_reference(args):
+    """The float64 CPU oracle, as it stands, on the machine's host cores."""
+    ws_, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    w = WORKLOADS[WORKLOAD]
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, budget_s=0.5)
+    vals = []
+    for _ in range(args.steps):
+        vals.append(cpu_oracle_sample(w, budget_s=max(2.0, 30.0 / max(1, args.steps))))
+    v = statistics.median(x["value"] for x in vals)
+    last = vals[-1]
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": ws_, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": {"workload": f"{WORKLOAD} (sampled rows on host cores)"},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
+                         "sample": last["sample"]},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="streamkl", choices=["streamkl", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(WORKLOADS),
+                    help="another named workload (the headline metric is quoted on 64k_causal)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl != "reference":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        out = run_reference(args)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    # the oracle's thread pool starts before any CUDA call
+    from oracle import oracle
+    oracle.build()
+    out, w = run_gpu(args)
+    ws_, rank, _ = dist_env()
+    if rank == 0:
+        if ws_ == 1 and not args.no_cpu:
+            out["cpu_baseline"] = cpu_oracle_sample(w)
+        print(json.dumps(out), flush=True)
+    if ws_ > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

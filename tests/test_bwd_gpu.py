@@ -1,0 +1,141 @@
+"""Backward parity: libstreamkl (CUDA, through the C ABI) vs the float64 oracle,
+both settings, fused (atomic dQ) and split (separate dQ / dK kernels) modes."""
+import numpy as np
+import pytest
+import torch
+
+from attention_kl_divergence_gb300 import WORKLOADS, make_g, make_qk, make_workload, streamkl
+from oracle import oracle
+from parity import assert_grad, grad_report
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+FUSED, SPLIT = streamkl.BWD_FUSED, streamkl.BWD_SPLIT
+
+
+def gpu_grads(setting, Q1, K1, Q2, K2, g, causal, mode):
+    KL, L1, L2 = streamkl.kl_fwd(Q1, K1, Q2, K2, causal=causal)
+    dQ, dK = streamkl.kl_bwd(setting, g, Q1, K1, Q2, K2, KL, L1, L2, causal=causal, mode=mode)
+    torch.cuda.synchronize()
+    return dQ, dK
+
+
+def check_full(setting, Q1, K1, Q2, K2, g, causal, mode):
+    dQ, dK = gpu_grads(setting, Q1, K1, Q2, K2, g, causal, mode)
+    rdQ, rdK = oracle.bwd(setting, g, Q1, K1, Q2, K2, causal=causal)
+    assert_grad(dQ, rdQ, f"dQ (setting {setting})")
+    assert_grad(dK, rdK, f"dK (setting {setting})")
+    return dQ, dK
+
+
+@pytest.mark.parametrize("setting", [1, 2])
+def test_tiny_workload(setting):
+    w = WORKLOADS["tiny"]
+    Q1, K1, Q2, K2 = make_workload(w, device=DEV)
+    g = make_g(w.B, w.H, w.Nq, w.g_value, device=DEV)
+    check_full(setting, Q1, K1, Q2, K2, g, w.causal, streamkl.BWD_AUTO)
+
+
+@pytest.mark.parametrize("mode", [FUSED, SPLIT])
+@pytest.mark.parametrize("setting", [1, 2])
+@pytest.mark.parametrize("B,H,Nq,Nk,causal", [
+    (1, 2, 256, 256, True),
+    (1, 1, 200, 333, False),
+    (2, 1, 130, 130, True),
+    (1, 2, 257, 1000, True),
+    (1, 1, 1, 700, False),
+    (1, 1, 64, 64, False),
+])
+def test_shapes_d128(B, H, Nq, Nk, causal, setting, mode):
+    Q1, K1, Q2, K2 = make_qk(B, H, Nq, Nk, 128, 0.4, seed=Nq * 3 + Nk, device=DEV)
+    g = torch.rand((B, H, Nq), device=DEV) + 0.5
+    check_full(setting, Q1, K1, Q2, K2, g, causal, mode)
+
+
+@pytest.mark.parametrize("setting", [1, 2])
+@pytest.mark.parametrize("B,H,Nq,Nk,causal", [(1, 2, 190, 190, True), (2, 1, 100, 300, False)])
+def test_shapes_d64_split(B, H, Nq, Nk, causal, setting):
+    Q1, K1, Q2, K2 = make_qk(B, H, Nq, Nk, 64, 0.5, seed=Nq + 11 * Nk, device=DEV)
+    g = torch.rand((B, H, Nq), device=DEV) + 0.5
+    assert streamkl.bwd_plan(Q1, K1, setting, causal).path == streamkl.PATH_BWD_SPLIT
+    check_full(setting, Q1, K1, Q2, K2, g, causal, streamkl.BWD_AUTO)
+
+
+def test_fused_and_split_agree():
+    Q1, K1, Q2, K2 = make_qk(1, 4, 384, 384, 128, 0.3, seed=3, device=DEV)
+    g = torch.full((1, 4, 384), 1.0 / 1536, device=DEV)
+    for setting in (1, 2):
+        a = gpu_grads(setting, Q1, K1, Q2, K2, g, True, FUSED)
+        b = gpu_grads(setting, Q1, K1, Q2, K2, g, True, SPLIT)
+        for x, y in zip(a, b):
+            cos, rel = grad_report(x, y)
+            assert cos > 0.99999 and rel < 1e-3
+
+
+@pytest.mark.parametrize("setting", [1, 2])
+def test_key_gradient_sums_to_zero(setting):
+    """sum_j dS[i, j] = 0 in both settings, so dK summed over keys vanishes."""
+    Q1, K1, Q2, K2 = make_qk(1, 2, 512, 512, 128, 0.3, seed=8, device=DEV)
+    g = torch.ones((1, 2, 512), device=DEV)
+    dQ, dK = gpu_grads(setting, Q1, K1, Q2, K2, g, True, streamkl.BWD_AUTO)
+    s = dK.double().sum(dim=2).abs().max()
+    assert float(s) <= 2e-3 * float(dK.double().abs().sum(dim=2).max())
+
+
+def test_identical_inputs_give_zero_gradients():
+    Q, K, _, _ = make_qk(1, 1, 300, 300, 128, 0.3, seed=4, device=DEV)
+    g = torch.ones((1, 1, 300), device=DEV)
+    for setting in (1, 2):
+        dQ, dK = gpu_grads(setting, Q, K, Q, K, g, True, streamkl.BWD_AUTO)
+        # P1 == P2 exactly in exact arithmetic; what remains is rounding
+        assert float(dQ.abs().max()) < 1e-3 and float(dK.abs().max()) < 1e-3
+
+
+def test_autograd_function():
+    Q1, K1, Q2, K2 = make_qk(1, 2, 200, 200, 128, 0.5, seed=2, device=DEV)
+    Q2.requires_grad_(True)
+    K2.requires_grad_(True)
+    KL = streamkl.AttentionKL.apply(Q1, K1, Q2, K2, True, None)
+    KL.sum().backward()
+    rdQ, rdK = oracle.bwd(1, np.ones((1, 2, 200)), Q1, K1, Q2.detach(), K2.detach(), causal=True)
+    assert_grad(Q2.grad.float(), rdQ, "dQ2 (autograd)")
+    assert_grad(K2.grad.float(), rdK, "dK2 (autograd)")
+
+
+def sample_keys(B, H, Nk, seed, n=64):
+    rng = np.random.default_rng(seed)
+    heads = [0, B * H - 1]
+    keys = []
+    for bh in heads:
+        js = set(rng.integers(Nk - 1024, Nk, size=n // 2).tolist()) | {0, 1, 127, 128, Nk // 2, Nk - 1}
+        keys += [bh * Nk + j for j in sorted(js)]
+    return np.array(keys, dtype=np.int64)
+
+
+def sample_rows(B, H, Nq, seed, n=256):
+    rng = np.random.default_rng(seed + 1)
+    rows = set(rng.integers(0, B * H * Nq, size=n).tolist()) | {0, 127, 128, Nq - 1, B * H * Nq - 1}
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def check_sampled_grads(w, setting, mode=streamkl.BWD_AUTO):
+    Q1, K1, Q2, K2 = make_workload(w, device=DEV)
+    g = make_g(w.B, w.H, w.Nq, w.g_value, device=DEV)
+    dQ, dK = gpu_grads(setting, Q1, K1, Q2, K2, g, w.causal, mode)
+    rows = sample_rows(w.B, w.H, w.Nq, w.seed)
+    keys = sample_keys(w.B, w.H, w.Nk, w.seed)
+    rdQ = oracle.bwd_dq_rows(setting, g, Q1, K1, Q2, K2, rows, causal=w.causal)
+    rdK = oracle.bwd_dk_keys(setting, g, Q1, K1, Q2, K2, keys, causal=w.causal)
+    gdQ = dQ.reshape(-1, w.d)[torch.as_tensor(rows, device=DEV)]
+    gdK = dK.reshape(-1, w.d)[torch.as_tensor(keys, device=DEV)]
+    assert_grad(gdQ, rdQ, f"dQ rows (setting {setting})")
+    assert_grad(gdK, rdK, f"dK keys (setting {setting})")
+    assert torch.isfinite(dQ).all() and torch.isfinite(dK).all()
+
+
+def test_8k_causal_setting1_sampled():
+    check_sampled_grads(WORKLOADS["8k_causal"], 1)
+
+
+def test_8k_causal_setting2_sampled():
+    check_sampled_grads(WORKLOADS["8k_causal"], 2)
