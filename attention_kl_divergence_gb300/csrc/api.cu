@@ -350,6 +350,60 @@ streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const flo
     return STREAMKL_OK;
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Forward without any allocation: the scratch lives in this file-scope device
+// array (every GPU that loads the library holds it until the process exits).
+// Host code only ever sees the array's host-side stand-in; its device address
+// comes from cudaGetSymbolAddress, looked up once per device below.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = STREAMKL_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (set-up on the
+// first call per device, with that device current).
+streamkl_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return STREAMKL_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return STREAMKL_ERR_CUDA;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return STREAMKL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+streamkl_status streamkl_fwd_noalloc(const streamkl_shape* shape, const void* Q1, const void* K1, const void* Q2,
+                                     const void* K2, float scale, int causal, float* KL, float* LSE1, float* LSE2,
+                                     const streamkl_options* opt, streamkl_stream_t stream) {
+    FwdPlan pl{};
+    streamkl_status st = plan_fwd(shape, causal, opt, &pl);
+    if (st != STREAMKL_OK) return st;
+    if (pl.ws_bytes > kNoAllocScratchBytes) return STREAMKL_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    if ((st = noalloc_scratch(&scratch)) != STREAMKL_OK) return st;
+    // the error word must start this call at zero; the partial states need no
+    // clearing (every one is written before the combine reads it)
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(scratch, 0, kStatusBytes, s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+    return streamkl_fwd(shape, Q1, K1, Q2, K2, scale, causal, KL, LSE1, LSE2, scratch, kNoAllocScratchBytes, opt,
+                        stream);
+}
+
 streamkl_status streamkl_workspace_status(void* workspace, streamkl_stream_t stream, uint32_t* device_error) {
     if (!workspace) return STREAMKL_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

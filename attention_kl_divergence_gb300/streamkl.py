@@ -49,7 +49,7 @@ class StreamKLError(RuntimeError):
 
 
 EXPORTED = ("streamkl_fwd_plan", "streamkl_fwd", "streamkl_bwd_plan", "streamkl_bwd", "streamkl_workspace_status",
-            "streamkl_status_string", "streamkl_version")
+            "streamkl_status_string", "streamkl_version", "streamkl_fwd_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -77,10 +77,11 @@ def load(build_if_stale: bool = True):
         lib.streamkl_bwd_plan.argtypes = [sp, I, I, op, pp]
         lib.streamkl_bwd.argtypes = [sp, I, P, P, P, P, P, P, P, P, F, I, P, P, P, Z, op, P]
         lib.streamkl_workspace_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
+        lib.streamkl_fwd_noalloc.argtypes = [sp, P, P, P, P, F, I, P, P, P, op, P]
         lib.streamkl_status_string.argtypes = [I]
         lib.streamkl_status_string.restype = ctypes.c_char_p
         for name in ("streamkl_fwd_plan", "streamkl_fwd", "streamkl_bwd_plan", "streamkl_bwd",
-                     "streamkl_workspace_status", "streamkl_version"):
+                     "streamkl_workspace_status", "streamkl_version", "streamkl_fwd_noalloc"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib

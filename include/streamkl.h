@@ -125,6 +125,34 @@ STREAMKL_API streamkl_status streamkl_bwd(const streamkl_shape* shape, int setti
                              const float* LSE2, float scale, int causal, float* dQ, float* dK, void* workspace,
                              size_t workspace_bytes, const streamkl_options* opt, streamkl_stream_t stream);
 
+/* Size of the library's own built-in scratch buffer used by streamkl_fwd_noalloc. */
+#define STREAMKL_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* Forward for callers that cannot allocate device memory themselves -- for
+ * example a host program or plugin that is handed tensor pointers by a
+ * runtime that owns all device memory and offers it no allocator, or a
+ * caller that must not allocate once its memory plan is fixed.  This entry
+ * point has no counterpart in the paper; it is streamkl_fwd with the
+ * workspace replaced by a fixed buffer that lives inside the library.
+ *
+ * Same arguments, outputs and validation as streamkl_fwd, minus the
+ * workspace.  Neither this call nor anything it launches allocates device
+ * memory: the scratch (the device error word plus the Split-K partial
+ * states) is a file-scope device array of STREAMKL_NOALLOC_SCRATCH_BYTES
+ * bytes that every GPU which loads the library holds until the process
+ * exits.  A shape whose plan needs more scratch than that (20 bytes per
+ * query row and key split, plus 256) returns STREAMKL_ERR_WORKSPACE and
+ * launches nothing.  The first call on a device looks up the array's device
+ * address (once per device, with that device current); make that first call
+ * before any stream capture.  Each call clears the error word it uses; all
+ * calls share the one array, so calls that may overlap on the GPU (different
+ * streams, or different host threads) race on it and must be serialised by
+ * the caller.  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+STREAMKL_API streamkl_status streamkl_fwd_noalloc(const streamkl_shape* shape, const void* Q1, const void* K1,
+                                                  const void* Q2, const void* K2, float scale, int causal, float* KL,
+                                                  float* LSE1, float* LSE2, const streamkl_options* opt,
+                                                  streamkl_stream_t stream);
+
 /* Synchronises `stream`, reads the workspace's device error word into
  * *device_error (if not NULL), clears it, and returns STREAMKL_ERR_TIMEOUT if
  * it was set, STREAMKL_OK otherwise (or CUDA on a failed copy). */
