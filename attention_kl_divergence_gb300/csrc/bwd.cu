@@ -24,6 +24,9 @@ namespace streamkl {
 namespace {
 
 constexpr int kBwdTile = 64;  // the inner (streamed) tile of both backward kernels
+// Bound of the waits that let in-flight TMA copies and MMAs retire before a CTA
+// exits (independent of the caller's wait limit).
+constexpr uint64_t kDrainNs = 200000000ull;
 
 __device__ __noinline__ bool drain_wait_b(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     uint64_t t0 = global_timer_ns();
@@ -195,8 +198,8 @@ __global__ void __launch_bounds__(320, 1)
                 }
             }
             for (int j = max(0, it - NST); j < it; ++j) {
-                drain_wait_b(base + L::bar_kfull + 8 * (j % NST), (j / NST) & 1, p.wait_ns);
-                drain_wait_b(base + L::bar_kempty + 8 * (j % NST), (j / NST) & 1, p.wait_ns / 8 + 1000000);
+                drain_wait_b(base + L::bar_kfull + 8 * (j % NST), (j / NST) & 1, kDrainNs);
+                if (!*abort_flag) drain_wait_b(base + L::bar_kempty + 8 * (j % NST), (j / NST) & 1, kDrainNs);
             }
         }
     } else if (warp == 1) {
@@ -205,6 +208,7 @@ __global__ void __launch_bounds__(320, 1)
             constexpr uint32_t id_dq = idesc_bf16_f32(kBlockQ, D, 0, 1);
             const uint32_t t_dq = tmem + 256;
             int issued = 0;
+            bool started = false;
             auto issue_s = [&](int it) {
                 const int s = it % NST, buf = it & 1;
                 const uint32_t k1s = base + L::k + 2 * s * L::kKBytes;
@@ -229,6 +233,7 @@ __global__ void __launch_bounds__(320, 1)
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
+                started = true;
                 for (int it = 0; it < n_tiles; ++it) {
                     if (it + 1 < n_tiles) {
                         const int n1 = it + 1;
@@ -257,7 +262,10 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 if (issued == n_tiles) tc_commit(base + L::bar_done);
             }
-            if (*abort_flag) drain_wait_b(base + L::bar_done, 0, p.wait_ns / 8 + 1000000);
+            if (*abort_flag && started) {  // let the issued MMAs retire before TMEM is freed
+                tc_commit(base + L::bar_done);
+                drain_wait_b(base + L::bar_done, 0, kDrainNs);
+            }
         }
     } else {
         // Two warpgroups: warps 2-5 take keys 0-31 of every tile, warps 6-9 keys 32-63.
@@ -467,8 +475,8 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
         }
         if (lane == 0) {
             for (int j = max(0, m - NST); j < m; ++j) {
-                drain_wait_b(base + L::bar_qfull + 8 * (j % NST), (j / NST) & 1, p.wait_ns);
-                drain_wait_b(base + L::bar_qempty + 8 * (j % NST), (j / NST) & 1, p.wait_ns / 8 + 1000000);
+                drain_wait_b(base + L::bar_qfull + 8 * (j % NST), (j / NST) & 1, kDrainNs);
+                if (!*abort_flag) drain_wait_b(base + L::bar_qempty + 8 * (j % NST), (j / NST) & 1, kDrainNs);
             }
         }
     } else if (warp == 1) {
@@ -498,11 +506,13 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
                 tc_commit(base + L::bar_sfull + 8 * buf);
             };
             int issued = 0;
+            bool started = false;
             bool ok = mbar_wait(base + L::bar_k, 0, wc, kErrWaitK) &&
                       mbar_wait(base + L::bar_qfull, 0, wc, kErrWaitQ);
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
+                started = true;
                 for (int m = 0; m < n_tiles; ++m) {
                     if (m + 1 < n_tiles) {
                         const int n1 = m + 1;
@@ -546,7 +556,10 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
                 }
                 if (issued == n_tiles) tc_commit(base + L::bar_done);
             }
-            if (*abort_flag) drain_wait_b(base + L::bar_done, 0, p.wait_ns / 8 + 1000000);
+            if (*abort_flag && started) {  // let the issued MMAs retire before TMEM is freed
+                tc_commit(base + L::bar_done);
+                drain_wait_b(base + L::bar_done, 0, kDrainNs);
+            }
         }
     } else if (warp < 10) {
         // ------------------------------------------------ recompute + dS^T

@@ -22,6 +22,9 @@ namespace streamkl {
 namespace {
 
 constexpr float kTau = 8.0f;  // lazy rescale: tolerate running maxima up to 2^8 stale
+// Bound of the waits that let in-flight TMA copies and MMAs retire before a CTA
+// exits (independent of the caller's wait limit).
+constexpr uint64_t kDrainNs = 200000000ull;
 
 // Shared-memory plan of the tile kernel.  Every operand tile starts on a
 // 1024-byte boundary (128-byte swizzle atoms of 8 rows).
@@ -39,7 +42,8 @@ struct TileSmem {
     static constexpr int bar_kempty = bar_kfull + 8 * NST;
     static constexpr int bar_sfull = bar_kempty + 8 * NST;
     static constexpr int bar_sempty = bar_sfull + 16;
-    static constexpr int misc = bar_sempty + 16;  // tmem base (4 B), abort flag (4 B)
+    static constexpr int bar_done = bar_sempty + 16;  // drain barrier of an aborted MMA issuer
+    static constexpr int misc = bar_done + 8;     // tmem base (4 B), abort flag (4 B)
     static constexpr int red = misc + 16;         // [5][128] floats: second warpgroup's row states
     static constexpr int total = red + 5 * 128 * 4;
     static constexpr int alloc = total + 1024;    // slack for 1024-byte alignment
@@ -55,17 +59,33 @@ __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t 
 
 // One 32-column chunk of a score row: online update of the five scalars.
 // MASKED: only columns e <= last are visible (causal frontier or key tail).
+// The unmasked path (every tile but the diagonal and tail ones) runs on packed
+// FP32x2 arithmetic and three-input maxima.
 template <bool MASKED>
 __device__ __forceinline__ void update_chunk(const float (&z1)[32], const float (&z2)[32], int last, RowState& st,
                                              float c, float tau) {
     if (MASKED && last < 0) return;  // the whole chunk lies beyond the row's last key
-    float cm1 = -INFINITY, cm2 = -INFINITY;
+    float cm1, cm2;
+    if (MASKED) {
+        cm1 = cm2 = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-        if (!MASKED || e <= last) {
-            cm1 = fmaxf(cm1, z1[e]);
-            cm2 = fmaxf(cm2, z2[e]);
+        for (int e = 0; e < 32; ++e) {
+            if (e <= last) {
+                cm1 = fmaxf(cm1, z1[e]);
+                cm2 = fmaxf(cm2, z2[e]);
+            }
         }
+    } else {
+        float a1 = -INFINITY, b1 = -INFINITY, a2 = -INFINITY, b2 = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+            a1 = max3f(a1, z1[e], z1[e + 1]);
+            b1 = max3f(b1, z1[e + 2], z1[e + 3]);
+            a2 = max3f(a2, z2[e], z2[e + 1]);
+            b2 = max3f(b2, z2[e + 2], z2[e + 3]);
+        }
+        cm1 = fmaxf(a1, b1);
+        cm2 = fmaxf(a2, b2);
     }
     if (cm1 > st.m1 + tau) {
         float a = ex2(c * (st.m1 - cm1));  // 0 on the first visible chunk (m1 = -inf)
@@ -80,24 +100,43 @@ __device__ __forceinline__ void update_chunk(const float (&z1)[32], const float 
     }
     if (MASKED && st.m1 == -INFINITY) return;  // nothing visible yet
     const float n1 = -c * st.m1, n2 = -c * st.m2;
-    float s1[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f}, sa[4] = {0.f, 0.f, 0.f, 0.f};
+    if (MASKED) {
+        float s1 = 0.f, s2 = 0.f, sa = 0.f;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-        float p1 = ex2(fmaf(z1[e], c, n1));
-        float p2 = ex2(fmaf(z2[e], c, n2));
-        float df = z1[e] - z2[e];
-        if (MASKED && e > last) {
-            p1 = 0.f;
-            p2 = 0.f;
-            df = 0.f;
+        for (int e = 0; e < 32; ++e) {
+            if (e <= last) {
+                const float p1 = ex2(fmaf(z1[e], c, n1));
+                s1 += p1;
+                s2 += ex2(fmaf(z2[e], c, n2));
+                sa = fmaf(p1, z1[e] - z2[e], sa);
+            }
         }
-        s1[e & 3] += p1;
-        s2[e & 3] += p2;
-        sa[e & 3] = fmaf(p1, df, sa[e & 3]);
+        st.l1 += s1;
+        st.l2 += s2;
+        st.acc += sa;
+        return;
     }
-    st.l1 += (s1[0] + s1[1]) + (s1[2] + s1[3]);
-    st.l2 += (s2[0] + s2[1]) + (s2[2] + s2[3]);
-    st.acc += (sa[0] + sa[1]) + (sa[2] + sa[3]);
+    const float2 cc = make_float2(c, c), nn1 = make_float2(n1, n1), nn2 = make_float2(n2, n2);
+    const float2 neg = make_float2(-1.f, -1.f);
+    float2 s1[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float2 s2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float2 sa[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+        const int k = (e >> 1) & 1;
+        const float2 u1 = make_float2(z1[e], z1[e + 1]), u2 = make_float2(z2[e], z2[e + 1]);
+        const float2 x1 = __ffma2_rn(u1, cc, nn1);
+        const float2 x2 = __ffma2_rn(u2, cc, nn2);
+        const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+        const float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+        const float2 df = __ffma2_rn(u2, neg, u1);  // z1 - z2
+        s1[k] = __fadd2_rn(s1[k], p1);
+        s2[k] = __fadd2_rn(s2[k], p2);
+        sa[k] = __ffma2_rn(p1, df, sa[k]);
+    }
+    st.l1 += (s1[0].x + s1[0].y) + (s1[1].x + s1[1].y);
+    st.l2 += (s2[0].x + s2[0].y) + (s2[1].x + s2[1].y);
+    st.acc += (sa[0].x + sa[0].y) + (sa[1].x + sa[1].y);
 }
 
 __device__ __forceinline__ void store_row(const FwdParams& p, size_t row, int split, const RowState& st,
@@ -168,6 +207,7 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(base + L::bar_sfull + 8 * s, 1);
             mbar_init(base + L::bar_sempty + 8 * s, 256);
         }
+        mbar_init(base + L::bar_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -209,8 +249,8 @@ __global__ void __launch_bounds__(320, 1)
             }
             // drain: every issued copy has landed and every stage was released
             for (int j = max(0, it - NST); j < it; ++j) {
-                drain_wait(base + L::bar_kfull + 8 * (j % NST), (j / NST) & 1, p.wait_ns);
-                drain_wait(base + L::bar_kempty + 8 * (j % NST), (j / NST) & 1, p.wait_ns / 8 + 1000000);
+                drain_wait(base + L::bar_kfull + 8 * (j % NST), (j / NST) & 1, kDrainNs);
+                if (!*abort_flag) drain_wait(base + L::bar_kempty + 8 * (j % NST), (j / NST) & 1, kDrainNs);
             }
         }
     } else if (warp == 1) {
@@ -244,9 +284,9 @@ __global__ void __launch_bounds__(320, 1)
                     ++issued;
                 }
             }
-            if (*abort_flag && issued > 0) {  // let the last MMAs retire before TMEM is freed
-                const int j = issued - 1;
-                drain_wait(base + L::bar_sfull + 8 * (j & 1), (j >> 1) & 1, p.wait_ns);
+            if (*abort_flag && issued > 0) {  // let the issued MMAs retire before TMEM is freed
+                tc_commit(base + L::bar_done);
+                drain_wait(base + L::bar_done, 0, kDrainNs);
             }
         }
     } else {
@@ -335,7 +375,8 @@ struct DecodeSmem {
     static constexpr int bar_kempty = bar_kfull + 8 * NST;
     static constexpr int bar_sfull = bar_kempty + 8 * NST;
     static constexpr int bar_sempty = bar_sfull + 16;
-    static constexpr int misc = bar_sempty + 16;
+    static constexpr int bar_done = bar_sempty + 16;
+    static constexpr int misc = bar_done + 8;
     static constexpr int red = misc + 16;                    // [4 warps][16 q][5] floats
     static constexpr int total = red + 4 * kDecodeMaxQ * 5 * 4;
     static constexpr int alloc = total + 1024;
@@ -373,6 +414,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_init(base + L::bar_sfull + 8 * s, 1);
             mbar_init(base + L::bar_sempty + 8 * s, 128);
         }
+        mbar_init(base + L::bar_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -412,8 +454,8 @@ __global__ void __launch_bounds__(192, 1)
                 }
             }
             for (int j = max(0, it - NST); j < it; ++j) {
-                drain_wait(base + L::bar_kfull + 8 * (j % NST), (j / NST) & 1, p.wait_ns);
-                drain_wait(base + L::bar_kempty + 8 * (j % NST), (j / NST) & 1, p.wait_ns / 8 + 1000000);
+                drain_wait(base + L::bar_kfull + 8 * (j % NST), (j / NST) & 1, kDrainNs);
+                if (!*abort_flag) drain_wait(base + L::bar_kempty + 8 * (j % NST), (j / NST) & 1, kDrainNs);
             }
         }
     } else if (warp == 1) {
@@ -447,8 +489,8 @@ __global__ void __launch_bounds__(192, 1)
                 }
             }
             if (*abort_flag && issued > 0) {
-                const int j = issued - 1;
-                drain_wait(base + L::bar_sfull + 8 * (j & 1), (j >> 1) & 1, p.wait_ns);
+                tc_commit(base + L::bar_done);
+                drain_wait(base + L::bar_done, 0, kDrainNs);
             }
         }
     } else {

@@ -263,11 +263,22 @@ def run_gpu(args):
         "bwd_setting2": {"ms": b2_ms, "tflops": f_bwd / b2_ms / 1e9, "frac_bf16_peak": f_bwd / b2_ms / 1e9 / peak_tf,
                          "mode": "fused" if bplan2.path == streamkl.PATH_BWD_FUSED else "split"},
     }
-    # Dominant single-launch kernel timed live: the forward tile kernel (one
-    # launch per forward call at this size); algorithmic 4*d flops per visible pair.
-    roofline = {"kernel": "fwd_tile_kernel", "bound": "tensor", "achieved": f_fwd / fwd_ms / 1e9, "peak": peak_tf,
-                "unit": "TFLOP/s", "frac": f_fwd / fwd_ms / 1e9 / peak_tf, "traffic": None,
-                "peak_source": f"bf16_tflops ({peak_src}, burst)"}
+    # Roofline of the dominant kernel (largest share of the step), timed live
+    # with CUDA events around its call on the launching stream.  Forward call =
+    # one fwd_tile_kernel launch (4*d flops per visible pair); fused backward
+    # call = dQ zero-fill + one bwd_kv_kernel launch carrying the whole backward
+    # (8*d flops per visible pair); split backward call = bwd_q + bwd_kv.
+    names = {"fwd": "fwd_tile_kernel" if fplan.path == 0 else "fwd_decode_kernel",
+             "bwd_setting1": "bwd_kv_kernel<setting 1, fused>" if bplan1.path == streamkl.PATH_BWD_FUSED
+             else "bwd_q_kernel + bwd_kv_kernel (setting 1)",
+             "bwd_setting2": "bwd_kv_kernel<setting 2, fused>" if bplan2.path == streamkl.PATH_BWD_FUSED
+             else "bwd_q_kernel + bwd_kv_kernel (setting 2)"}
+    top = max(kernels, key=lambda k: kernels[k]["ms"])
+    flops_top = f_fwd if top == "fwd" else f_bwd
+    achieved = flops_top / kernels[top]["ms"] / 1e9
+    roofline = {"kernel": names[top], "bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved / peak_tf, "traffic": None, "share_of_step": kernels[top]["ms"] / step_ms,
+                "flops_per_launch": flops_top, "peak_source": f"bf16_tflops ({peak_src}, burst)"}
 
     # ---------------- end to end through the C ABI with host buffers
     pin = dict(pin_memory=True)
