@@ -74,7 +74,8 @@ struct FwdPlan {
 streamkl_status plan_fwd(const streamkl_shape* s, int causal, const streamkl_options* opt, FwdPlan* pl) {
     streamkl_status st = check_shape(s, causal);
     if (st != STREAMKL_OK) return st;
-    if (opt && opt->num_splits < 0) return STREAMKL_ERR_INVALID_ARG;
+    if (opt && (opt->num_splits < 0 || opt->reserved != 0 || (opt->debug_flags & ~STREAMKL_DEBUG_INJECT_STALL)))
+        return STREAMKL_ERR_INVALID_ARG;
     int sms = 0;
     if ((st = device_sms(&sms)) != STREAMKL_OK) return st;
     const int64_t BH = int64_t(s->B) * s->H;
@@ -117,6 +118,7 @@ streamkl_status plan_bwd(const streamkl_shape* s, int setting, int causal, const
     if (setting != 1 && setting != 2) return STREAMKL_ERR_INVALID_ARG;
     const int mode = opt ? opt->bwd_mode : 0;
     if (mode < 0 || mode > 2) return STREAMKL_ERR_INVALID_ARG;
+    if (opt && (opt->reserved != 0 || (opt->debug_flags & ~STREAMKL_DEBUG_INJECT_STALL))) return STREAMKL_ERR_INVALID_ARG;
     if (mode == 1 && s->d != 128) return STREAMKL_ERR_UNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
@@ -251,6 +253,7 @@ streamkl_status streamkl_fwd(const streamkl_shape* shape, const void* Q1, const 
     p.part = pl.num_splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes) : nullptr;
     p.status = static_cast<unsigned int*>(workspace);
     p.wait_ns = static_cast<unsigned long long>(wait_limit(opt));
+    p.inject_stall = (opt && (opt->debug_flags & STREAMKL_DEBUG_INJECT_STALL)) ? 1 : 0;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = pl.decode ? launch_fwd_decode(shape->d, maps, p, pl.ctas, s)
@@ -322,6 +325,7 @@ streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const flo
     p.dK = dK;
     p.status = static_cast<unsigned int*>(workspace);
     p.wait_ns = static_cast<unsigned long long>(wait_limit(opt));
+    p.inject_stall = (opt && (opt->debug_flags & STREAMKL_DEBUG_INJECT_STALL)) ? 1 : 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     // key-tile kernel: Q boxes of 64 rows, K boxes of 128 rows

@@ -197,6 +197,7 @@ __global__ void __launch_bounds__(320, 1)
                     tma_load_4d_hint(k2s + c * kBwdTile * 128, &tK2, fb, c * kSwizzleCols, k0, h, b, keep);
                 }
             }
+            drain_wait_b(base + L::bar_q, 0, kDrainNs);  // the query tiles' copies have landed
             for (int j = max(0, it - NST); j < it; ++j) {
                 drain_wait_b(base + L::bar_kfull + 8 * (j % NST), (j / NST) & 1, kDrainNs);
                 if (!*abort_flag) drain_wait_b(base + L::bar_kempty + 8 * (j % NST), (j / NST) & 1, kDrainNs);
@@ -228,7 +229,10 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 tc_commit(base + L::bar_sfull + 8 * buf);
             };
-            bool ok = mbar_wait(base + L::bar_q, 0, wc, kErrWaitQ) &&
+            // test aid: a wait on a barrier that nothing arrives on before the end
+            const bool stalled = p.inject_stall && blockIdx.x == 0 &&
+                                 !mbar_wait(base + L::bar_done, 0, wc, kErrWaitOther);
+            bool ok = !stalled && mbar_wait(base + L::bar_q, 0, wc, kErrWaitQ) &&
                       mbar_wait(base + L::bar_kfull, 0, wc, kErrWaitK);
             if (ok) {
                 tc_fence_after();
@@ -474,6 +478,7 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
             mbar_arrive(fb);
         }
         if (lane == 0) {
+            drain_wait_b(base + L::bar_k, 0, kDrainNs);  // the key tiles' copies have landed
             for (int j = max(0, m - NST); j < m; ++j) {
                 drain_wait_b(base + L::bar_qfull + 8 * (j % NST), (j / NST) & 1, kDrainNs);
                 if (!*abort_flag) drain_wait_b(base + L::bar_qempty + 8 * (j % NST), (j / NST) & 1, kDrainNs);
@@ -507,7 +512,10 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
             };
             int issued = 0;
             bool started = false;
-            bool ok = mbar_wait(base + L::bar_k, 0, wc, kErrWaitK) &&
+            // test aid: a wait on a barrier that nothing arrives on before the end
+            const bool stalled = p.inject_stall && blockIdx.x == 0 &&
+                                 !mbar_wait(base + L::bar_done, 0, wc, kErrWaitOther);
+            bool ok = !stalled && mbar_wait(base + L::bar_k, 0, wc, kErrWaitK) &&
                       mbar_wait(base + L::bar_qfull, 0, wc, kErrWaitQ);
             if (ok) {
                 tc_fence_after();

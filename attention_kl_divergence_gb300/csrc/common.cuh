@@ -20,6 +20,7 @@ constexpr uint32_t kErrWaitQ = 1u << 0;      // Q tile never arrived
 constexpr uint32_t kErrWaitK = 1u << 1;      // K tile never arrived / stage never freed
 constexpr uint32_t kErrWaitS = 1u << 2;      // score tile never produced / consumed
 constexpr uint32_t kErrWaitOther = 1u << 3;  // any other barrier
+constexpr uint32_t kErrSmemAlign = 1u << 4;  // dynamic shared memory not 1024-byte aligned
 
 // Forward (tile kernel and decode kernel share this block).
 struct FwdParams {
@@ -37,6 +38,7 @@ struct FwdParams {
     float* part;         // partial states [5][num_splits][B*H*Nq] when num_splits > 1
     unsigned int* status;
     unsigned long long wait_ns;
+    int inject_stall;    // CTA 0's MMA issuer waits on a barrier nothing arrives on
 };
 
 // Backward (both kernels).  Tile counts are in the kernel's own tile units.
@@ -56,6 +58,7 @@ struct BwdParams {
     float* dK;           // [B*H*Nk, d]
     unsigned int* status;
     unsigned long long wait_ns;
+    int inject_stall;
 };
 
 // Combine of Split-K partial states.

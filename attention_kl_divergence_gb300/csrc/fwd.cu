@@ -248,6 +248,7 @@ __global__ void __launch_bounds__(320, 1)
                 }
             }
             // drain: every issued copy has landed and every stage was released
+            drain_wait(base + L::bar_q, 0, kDrainNs);  // the query tiles' copies have landed
             for (int j = max(0, it - NST); j < it; ++j) {
                 drain_wait(base + L::bar_kfull + 8 * (j % NST), (j / NST) & 1, kDrainNs);
                 if (!*abort_flag) drain_wait(base + L::bar_kempty + 8 * (j % NST), (j / NST) & 1, kDrainNs);
@@ -258,7 +259,11 @@ __global__ void __launch_bounds__(320, 1)
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(kBlockQ, kBlockK);
             int issued = 0;
-            if (mbar_wait(base + L::bar_q, 0, wc, kErrWaitQ)) {
+            // test aid: a wait on a barrier that nothing arrives on (bar_done is
+            // only committed on the abort path below) gives up after wait_ns
+            const bool stalled = p.inject_stall && blockIdx.x == 0 &&
+                                 !mbar_wait(base + L::bar_done, 0, wc, kErrWaitOther);
+            if (!stalled && mbar_wait(base + L::bar_q, 0, wc, kErrWaitQ)) {
                 tc_fence_after();
                 for (int it = 0; it < n_tiles; ++it) {
                     const int s = it % NST, buf = it & 1;
@@ -453,6 +458,7 @@ __global__ void __launch_bounds__(192, 1)
                     tma_load_4d_hint(k2s + c * kBlockK * 128, &tK2, fb, c * kSwizzleCols, k0, h, b, stream_once);
                 }
             }
+            drain_wait(base + L::bar_q, 0, kDrainNs);  // the query tiles' copies have landed
             for (int j = max(0, it - NST); j < it; ++j) {
                 drain_wait(base + L::bar_kfull + 8 * (j % NST), (j / NST) & 1, kDrainNs);
                 if (!*abort_flag) drain_wait(base + L::bar_kempty + 8 * (j % NST), (j / NST) & 1, kDrainNs);
@@ -462,7 +468,11 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(kBlockK, NQ);
             int issued = 0;
-            if (mbar_wait(base + L::bar_q, 0, wc, kErrWaitQ)) {
+            // test aid: a wait on a barrier that nothing arrives on (bar_done is
+            // only committed on the abort path below) gives up after wait_ns
+            const bool stalled = p.inject_stall && blockIdx.x == 0 &&
+                                 !mbar_wait(base + L::bar_done, 0, wc, kErrWaitOther);
+            if (!stalled && mbar_wait(base + L::bar_q, 0, wc, kErrWaitQ)) {
                 tc_fence_after();
                 for (int it = 0; it < n_tiles; ++it) {
                     const int s = it % NST, buf = it & 1;

@@ -34,7 +34,11 @@ class Shape(ctypes.Structure):
 
 
 class Options(ctypes.Structure):
-    _fields_ = [("num_splits", ctypes.c_int32), ("bwd_mode", ctypes.c_int32), ("wait_limit_ns", ctypes.c_int64)]
+    _fields_ = [("num_splits", ctypes.c_int32), ("bwd_mode", ctypes.c_int32), ("wait_limit_ns", ctypes.c_int64),
+                ("debug_flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+DEBUG_INJECT_STALL = 1
 
 
 class Plan(ctypes.Structure):
@@ -126,8 +130,8 @@ def _check_qk(Q1, K1, Q2, K2):
         raise ValueError("Q and K must share B, H and d")
 
 
-def _opts(num_splits=0, bwd_mode=0, wait_limit_ns=0):
-    return Options(int(num_splits), int(bwd_mode), int(wait_limit_ns))
+def _opts(num_splits=0, bwd_mode=0, wait_limit_ns=0, debug_flags=0):
+    return Options(int(num_splits), int(bwd_mode), int(wait_limit_ns), int(debug_flags), 0)
 
 
 def fwd_plan(Q1, K1, causal=False, num_splits=0) -> Plan:
@@ -150,12 +154,12 @@ def new_workspace(nbytes, device) -> torch.Tensor:
 
 
 def kl_fwd(Q1, K1, Q2, K2, causal=False, scale=None, num_splits=0, workspace=None, out=None,
-           wait_limit_ns=0):
+           wait_limit_ns=0, debug_flags=0):
     """Per-row KL(P1 || P2), LSE1, LSE2 as float32 [B, H, Nq] tensors."""
     _check_qk(Q1, K1, Q2, K2)
     lib = load()
     shape = make_shape(Q1, K1)
-    opts = _opts(num_splits, 0, wait_limit_ns)
+    opts = _opts(num_splits, 0, wait_limit_ns, debug_flags)
     plan = Plan()
     _raise(lib.streamkl_fwd_plan(ctypes.byref(shape), int(bool(causal)), ctypes.byref(opts), ctypes.byref(plan)),
            "streamkl_fwd_plan")
@@ -174,12 +178,12 @@ def kl_fwd(Q1, K1, Q2, K2, causal=False, scale=None, num_splits=0, workspace=Non
 
 
 def kl_bwd(setting, g, Q1, K1, Q2, K2, KL, LSE1, LSE2, causal=False, scale=None, mode=BWD_AUTO, workspace=None,
-           out=None, wait_limit_ns=0):
+           out=None, wait_limit_ns=0, debug_flags=0):
     """(dQ, dK) float32 of the trainable side: setting 1 -> (Q2, K2), 2 -> (Q1, K1)."""
     _check_qk(Q1, K1, Q2, K2)
     lib = load()
     shape = make_shape(Q1, K1)
-    opts = _opts(0, mode, wait_limit_ns)
+    opts = _opts(0, mode, wait_limit_ns, debug_flags)
     plan = Plan()
     _raise(lib.streamkl_bwd_plan(ctypes.byref(shape), int(setting), int(bool(causal)), ctypes.byref(opts),
                                  ctypes.byref(plan)), "streamkl_bwd_plan")

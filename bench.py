@@ -35,6 +35,7 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from attention_kl_divergence_gb300 import WORKLOADS, make_g, make_workload  # noqa: E402
+from attention_kl_divergence_gb300.dist import barrier, env as dist_env, init as init_dist, max_over_ranks  # noqa: E402
 
 WORKLOAD = "64k_causal"
 METRIC = "fwd/bwd TFLOP/s and ms at 64K causal, fraction of GB300 BF16 tensor peak"
@@ -48,31 +49,6 @@ def load_peaks():
             d = json.load(f)
         return d, "measured"
     return dict(PEAKS_FALLBACK), "fallback"
-
-
-def dist_env():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
-
-
-def init_dist(ws, backend):
-    if ws > 1 and not torch.distributed.is_initialized():
-        torch.distributed.init_process_group(backend=backend)
-
-
-def barrier(ws):
-    if ws > 1:
-        torch.distributed.barrier()
-
-
-def max_over_ranks(x, ws, device):
-    if ws == 1:
-        return x
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    return float(t.item())
 
 
 class ClockSampler:

@@ -81,7 +81,15 @@ typedef struct {
     int32_t bwd_mode;      /* backward: 0 = automatic, 1 = fused (atomic dQ),        */
                            /*           2 = separate dQ and dK kernels                */
     int64_t wait_limit_ns; /* limit of every in-kernel wait; 0 = default (2 s)      */
+    int32_t debug_flags;   /* 0 in normal use; see STREAMKL_DEBUG_*                  */
+    int32_t reserved;      /* must be 0                                              */
 } streamkl_options;
+
+/* Test aid for the bounded waits: the first CTA of the main kernel waits on a
+ * barrier that nothing arrives on.  The wait gives up after wait_limit_ns,
+ * the kernel records STREAMKL_ERR_TIMEOUT in the workspace error word and
+ * returns; the outputs of that call are undefined. */
+#define STREAMKL_DEBUG_INJECT_STALL 1
 
 /* What a call will launch for a given shape (filled by the plan queries). */
 typedef struct {

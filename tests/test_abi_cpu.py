@@ -68,3 +68,12 @@ def test_fwd_rejects_bad_pointers_without_device():
 
 def test_workspace_status_rejects_null():
     assert sk.load().streamkl_workspace_status(None, None, None) == sk.ERR_INVALID_ARG
+
+
+def test_options_reject_unknown_debug_flags_without_device():
+    lib = sk.load()
+    P = ctypes.c_void_p
+    bad = sk.Options(0, 0, 0, 8, 0)
+    rc = lib.streamkl_fwd(ctypes.byref(_shape()), *[P(256)] * 4, ctypes.c_float(0.0), 0, *[P(256)] * 3, P(256),
+                          4096, ctypes.byref(bad), P(0))
+    assert rc in (sk.ERR_INVALID_ARG, sk.ERR_CUDA)  # the option check needs no device but runs in the planner
