@@ -31,11 +31,17 @@ class Workload:
     causal: bool
     teacher_scale: float = 1.0
     seed: int = 0
+    fwd_only: bool = False  # the decode (Split-K) workloads run the forward only
 
     @property
     def g_value(self) -> float:
         """Upstream gradient per row: 1 for the tiny case, 1/(H*Nq) otherwise."""
         return 1.0 if self.name == "tiny" else 1.0 / (self.H * self.Nq)
+
+    def fwd_bytes(self) -> int:
+        """Algorithmic HBM bytes of one forward: every Q and K element read once
+        (bf16) and KL, LSE1, LSE2 written once (float32)."""
+        return 2 * 2 * self.B * self.H * (self.Nq + self.Nk) * self.d + 12 * self.B * self.H * self.Nq
 
     def visible_pairs(self) -> int:
         """Query/key pairs inside the mask, per head.  Causal rows are aligned
@@ -52,10 +58,13 @@ WORKLOADS = {
     "8k_causal": Workload("8k_causal", 1, 32, 8192, 8192, 128, 0.3, True, seed=1),
     "64k_causal": Workload("64k_causal", 1, 32, 65536, 65536, 128, 0.3, True, seed=2),
     "64k": Workload("64k", 1, 32, 65536, 65536, 128, 0.3, False, seed=2),
-    "decode_q1_k128k": Workload("decode_q1_k128k", 4, 32, 1, 131072, 128, 0.3, False, seed=3),
-    "decode_q16_k128k": Workload("decode_q16_k128k", 4, 32, 16, 131072, 128, 0.3, False, seed=3),
-    "decode_q1_k512k": Workload("decode_q1_k512k", 4, 32, 1, 524288, 128, 0.3, False, seed=3),
-    "decode_q16_k512k": Workload("decode_q16_k512k", 4, 32, 16, 524288, 128, 0.3, False, seed=3),
+    "decode_q1_k128k": Workload("decode_q1_k128k", 4, 32, 1, 131072, 128, 0.3, False, seed=3, fwd_only=True),
+    "decode_q16_k128k": Workload("decode_q16_k128k", 4, 32, 16, 131072, 128, 0.3, False, seed=3, fwd_only=True),
+    "decode_q1_k512k": Workload("decode_q1_k512k", 4, 32, 1, 524288, 128, 0.3, False, seed=3, fwd_only=True),
+    "decode_q16_k512k": Workload("decode_q16_k512k", 4, 32, 16, 524288, 128, 0.3, False, seed=3, fwd_only=True),
+    # one batch of the 128K decode: small enough for a full ncu capture (2 GiB of keys)
+    "decode_q1_k128k_b1": Workload("decode_q1_k128k_b1", 1, 32, 1, 131072, 128, 0.3, False, seed=3,
+                                   fwd_only=True),
     "512k_causal": Workload("512k_causal", 1, 8, 524288, 524288, 128, 0.3, True, teacher_scale=1.5, seed=4),
 }
 

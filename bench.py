@@ -42,6 +42,21 @@ METRIC = "fwd/bwd TFLOP/s and ms at 64K causal, fraction of GB300 BF16 tensor pe
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# DRAM bytes (read + write) per launch of the dominant kernel, from ncu
+# (dram__bytes_read.sum + dram__bytes_write.sum) on the same command
+# (profiles/dram_64k_causal.md).  Keyed by (workload, pass) and valid only for the kernel
+# version they were taken on: reset to None whenever that kernel changes.
+TRAFFIC = {
+    ("64k_causal", "fwd"): 2.17e9 + 0.038e9,
+    ("64k_causal", "bwd_setting1"): 3.32e9 + 2.22e9,
+    ("64k_causal", "bwd_setting2"): 3.33e9 + 2.22e9,
+}
+
+
+def traffic_for(workload, which):
+    return TRAFFIC.get((workload, which))
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -173,7 +188,8 @@ def run_gpu(args):
     B, H, Nq, Nk, d = w.B, w.H, w.Nq, w.Nk, w.d
     f32 = dict(dtype=torch.float32, device=dev)
     KL, L1, L2 = (torch.empty((B, H, Nq), **f32) for _ in range(3))
-    dQ, dK = torch.empty((B, H, Nq, d), **f32), torch.empty((B, H, Nk, d), **f32)
+    dQ = torch.empty((B, H, Nq, d), **f32) if not w.fwd_only else None
+    dK = torch.empty((B, H, Nk, d), **f32) if not w.fwd_only else None
     fplan = streamkl.fwd_plan(Q1, K1, causal=w.causal)
     bplan1 = streamkl.bwd_plan(Q1, K1, 1, causal=w.causal)
     bplan2 = streamkl.bwd_plan(Q1, K1, 2, causal=w.causal)
@@ -187,14 +203,21 @@ def run_gpu(args):
     def bwd(setting):
         streamkl.kl_bwd(setting, g, Q1, K1, Q2, K2, KL, L1, L2, causal=w.causal, workspace=wsp, out=(dQ, dK))
 
-    launches_per_step = fplan.launches + bplan1.launches + bplan2.launches
-    if bplan1.path == streamkl.PATH_BWD_FUSED:
+    with_bwd = not w.fwd_only
+    launches_per_step = fplan.launches + ((bplan1.launches + bplan2.launches) if with_bwd else 0)
+    if with_bwd and bplan1.path == streamkl.PATH_BWD_FUSED:
         launches_per_step -= 1  # the dQ zero-fill is a memset, not one of our kernels
-    if bplan2.path == streamkl.PATH_BWD_FUSED:
+    if with_bwd and bplan2.path == streamkl.PATH_BWD_FUSED:
         launches_per_step -= 1
 
+    def step():
+        fwd()
+        if with_bwd:
+            bwd(1)
+            bwd(2)
+
     for _ in range(args.warmup):
-        fwd(), bwd(1), bwd(2)
+        step()
     torch.cuda.synchronize()
     if streamkl.workspace_status(wsp):
         raise RuntimeError("device error word set during warm-up")
@@ -203,20 +226,18 @@ def run_gpu(args):
     barrier(ws_)
     torch.cuda.synchronize()
     with ClockSampler(gpu_id(dev)) as clk:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
         for k in range(args.steps):
             flush_l2(l2_flush)
             e = ev[k]
             e[0].record(stream)
             fwd()
             e[1].record(stream)
-            bwd(1)
+            if with_bwd:
+                bwd(1)
             e[2].record(stream)
-            bwd(2)
+            if with_bwd:
+                bwd(2)
             e[3].record(stream)
-        t_end.record(stream)
         torch.cuda.synchronize()
     barrier(ws_)
     status = streamkl.workspace_status(wsp)
@@ -228,33 +249,45 @@ def run_gpu(args):
 
     pairs = w.visible_pairs() * B * H
     f_fwd, f_bwd = 4 * d * pairs, 8 * d * pairs
-    step_flops = f_fwd + 2 * f_bwd
+    step_flops = f_fwd + (2 * f_bwd if with_bwd else 0)
     value = step_flops * ws_ / (step_ms * 1e-3) / 1e12
     peak_tf = peaks["bf16_tflops"]
-    kernels = {
-        "fwd": {"ms": fwd_ms, "tflops": f_fwd / fwd_ms / 1e9, "frac_bf16_peak": f_fwd / fwd_ms / 1e9 / peak_tf,
-                "path": "tile" if fplan.path == 0 else "decode", "splits": fplan.num_splits},
-        "bwd_setting1": {"ms": b1_ms, "tflops": f_bwd / b1_ms / 1e9, "frac_bf16_peak": f_bwd / b1_ms / 1e9 / peak_tf,
-                         "mode": "fused" if bplan1.path == streamkl.PATH_BWD_FUSED else "split"},
-        "bwd_setting2": {"ms": b2_ms, "tflops": f_bwd / b2_ms / 1e9, "frac_bf16_peak": f_bwd / b2_ms / 1e9 / peak_tf,
-                         "mode": "fused" if bplan2.path == streamkl.PATH_BWD_FUSED else "split"},
-    }
+    kernels = {"fwd": {"ms": fwd_ms, "tflops": f_fwd / fwd_ms / 1e9, "frac_bf16_peak": f_fwd / fwd_ms / 1e9 / peak_tf,
+                       "gbs": w.fwd_bytes() / fwd_ms / 1e6, "frac_hbm_peak": w.fwd_bytes() / fwd_ms / 1e6 /
+                       peaks["hbm_gbs"], "path": "tile" if fplan.path == 0 else "decode",
+                       "splits": fplan.num_splits}}
+    if with_bwd:
+        kernels["bwd_setting1"] = {"ms": b1_ms, "tflops": f_bwd / b1_ms / 1e9,
+                                   "frac_bf16_peak": f_bwd / b1_ms / 1e9 / peak_tf,
+                                   "mode": "fused" if bplan1.path == streamkl.PATH_BWD_FUSED else "split"}
+        kernels["bwd_setting2"] = {"ms": b2_ms, "tflops": f_bwd / b2_ms / 1e9,
+                                   "frac_bf16_peak": f_bwd / b2_ms / 1e9 / peak_tf,
+                                   "mode": "fused" if bplan2.path == streamkl.PATH_BWD_FUSED else "split"}
     # Roofline of the dominant kernel (largest share of the step), timed live
     # with CUDA events around its call on the launching stream.  Forward call =
-    # one fwd_tile_kernel launch (4*d flops per visible pair); fused backward
-    # call = dQ zero-fill + one bwd_kv_kernel launch carrying the whole backward
-    # (8*d flops per visible pair); split backward call = bwd_q + bwd_kv.
-    names = {"fwd": "fwd_tile_kernel" if fplan.path == 0 else "fwd_decode_kernel",
+    # one fwd_tile_kernel launch (4*d flops per visible pair), or for decode one
+    # fwd_decode_kernel + combine launch bounded by HBM (every Q/K byte once);
+    # fused backward call = dQ zero-fill + one bwd_kv_kernel launch carrying the
+    # whole backward (8*d flops per visible pair); split = bwd_q + bwd_kv.
+    names = {"fwd": "fwd_tile_kernel" if fplan.path == 0 else "fwd_decode_kernel + combine_kernel",
              "bwd_setting1": "bwd_kv_kernel<setting 1, fused>" if bplan1.path == streamkl.PATH_BWD_FUSED
              else "bwd_q_kernel + bwd_kv_kernel (setting 1)",
              "bwd_setting2": "bwd_kv_kernel<setting 2, fused>" if bplan2.path == streamkl.PATH_BWD_FUSED
              else "bwd_q_kernel + bwd_kv_kernel (setting 2)"}
     top = max(kernels, key=lambda k: kernels[k]["ms"])
-    flops_top = f_fwd if top == "fwd" else f_bwd
-    achieved = flops_top / kernels[top]["ms"] / 1e9
-    roofline = {"kernel": names[top], "bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": achieved / peak_tf, "traffic": None, "share_of_step": kernels[top]["ms"] / step_ms,
-                "flops_per_launch": flops_top, "peak_source": f"bf16_tflops ({peak_src}, burst)"}
+    if top == "fwd" and fplan.path == streamkl.PATH_DECODE:
+        achieved = w.fwd_bytes() / fwd_ms / 1e6
+        roofline = {"kernel": names[top], "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_for(w.name, top),
+                    "share_of_step": kernels[top]["ms"] / step_ms, "bytes_per_launch": w.fwd_bytes(),
+                    "peak_source": f"hbm_gbs ({peak_src})"}
+    else:
+        flops_top = f_fwd if top == "fwd" else f_bwd
+        achieved = flops_top / kernels[top]["ms"] / 1e9
+        roofline = {"kernel": names[top], "bound": "tensor", "achieved": achieved, "peak": peak_tf,
+                    "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic_for(w.name, top),
+                    "share_of_step": kernels[top]["ms"] / step_ms, "flops_per_launch": flops_top,
+                    "peak_source": f"bf16_tflops ({peak_src}, burst)"}
 
     # ---------------- end to end through the C ABI with host buffers
     pin = dict(pin_memory=True)
@@ -268,7 +301,7 @@ def run_gpu(args):
         Q1.copy_(hQ1, non_blocking=True), K1.copy_(hK1, non_blocking=True)
         Q2.copy_(hQ2, non_blocking=True), K2.copy_(hK2, non_blocking=True)
         g.copy_(hg, non_blocking=True)
-        fwd(), bwd(1), bwd(2)
+        step()
         hKL.copy_(KL, non_blocking=True)
 
     e2e_step()
@@ -292,8 +325,10 @@ def run_gpu(args):
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) teacher, student +0.3 N(0,1))",
             "config": {"workload": f"{w.name}: B={B} H={H} N_Q={Nq} N_K={Nk} d={d} "
-                                   f"{'causal' if w.causal else 'non-causal'}, fwd + bwd setting 1 + "
-                                   f"bwd setting 2 per step", "l2": "256 MB write between steps",
+                                   f"{'causal' if w.causal else 'non-causal'}, "
+                                   + ("fwd only (Split-K decode) per step" if w.fwd_only else
+                                      "fwd + bwd setting 1 + bwd setting 2 per step"),
+                       "l2": "256 MB write between steps",
                        "parallelism": f"heads-independent replicas x{ws_}"},
             "kernels": kernels, "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "device_error_word": status, "kl_mean": kl_mean,
