@@ -12,7 +12,8 @@
 //   bwd_q_kernel   one 128-row query tile; loops over 64-key tiles; dQ in TMEM.
 //   bwd_kv_kernel  one 128-key tile; loops over 64-row query tiles; dK in TMEM.
 //                  FUSED also forms dQ^T = K_t^T dS^T per tile pair and adds it
-//                  to global dQ with atomics (each QK tile pair visited once).
+//                  to global dQ with bulk L2 reductions (each QK tile pair
+//                  visited once).
 // The split mode runs both kernels (each recomputes the scores); the fused
 // mode runs bwd_kv_kernel<FUSED> alone after zeroing dQ.
 #include "common.cuh"
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(320, 1)
                         tc_fence_after();
                         issue_s(n1);
                     }
-                    const int s = it % NST, buf = it & 1;
+                    const int s = it % NST;
                     const int dsb = it % L::kNumDs;
                     if (!mbar_wait(base + L::bar_dsfull + 8 * dsb, (it / L::kNumDs) & 1, wc, kErrWaitOther)) break;
                     tc_fence_after();
@@ -352,8 +353,12 @@ __global__ void __launch_bounds__(320, 1)
 // bwd_kv: CTA = 128 keys; 64-row query tiles streamed through a 3-stage ring.
 // Warps: 0 TMA + per-row constants, 1 TMEM + MMA, 2-9 recompute/dS (two
 // warpgroups, one key per thread, each taking 32 of the tile's 64 query rows),
-// 10-13 (FUSED) dQ^T accumulator -> global atomics.
-// TMEM: S1^T|S2^T double buffered (cols 0-255), dK (256-383), dQ^T x2 (384-511).
+// 10-13 (FUSED) dQ^T accumulator -> bulk reduce-add into global dQ.
+// TMEM: K1|K2 as the A operand of the score MMAs (cols 0-127, copied in once),
+// S1^T|S2^T (128-255, one buffer, released as soon as the update warps hold it
+// in registers), dK (256-383), dQ^T for the hi|lo halves of dS (384-511).
+// An M = 128 MMA reading A from shared memory costs ~90 cycles whatever N <= 128
+// is; with A in tensor memory an N = 128 MMA runs at the full rate.
 // ---------------------------------------------------------------------------
 template <int D, int NST>
 struct KvSmem {
@@ -363,7 +368,7 @@ struct KvSmem {
     static constexpr int k1 = 0;
     static constexpr int k2 = kKBytes;
     static constexpr int q = 2 * kKBytes;
-    static constexpr int kNumDs = 1;                   // dS buffers: the update computes before it stores
+    static constexpr int kNumDs = 2;                   // dS buffers (hi + lo each)
     static constexpr int ds = q + 2 * NST * kQBytes;   // buffer b: hi at ds + 2*b*kDsBytes, lo right after
     static constexpr int vec = ds + 2 * kNumDs * kDsBytes;  // [NST][3][64] floats
     static constexpr int bars = vec + NST * 3 * kBwdTile * 4;
@@ -379,7 +384,7 @@ struct KvSmem {
     static constexpr int bar_done = bar_dqempty + 16;
     static constexpr int misc = bar_done + 8;
     static constexpr int total = misc + 16;
-    static constexpr int alloc = total + 1024;
+    static constexpr int alloc = total;  // no slack: the kernel checks the base is 1024-byte aligned
 };
 
 template <int D, int NST, int SETTING, bool FUSED>
@@ -388,9 +393,16 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
                   const __grid_constant__ CUtensorMap tQ2, const __grid_constant__ CUtensorMap tK2,
                   const BwdParams p) {
     using L = KvSmem<D, NST>;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    uint8_t* gbase = smem_raw + (base - smem_u32(smem_raw));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // The layout uses every byte it asked for, so the dynamic shared memory
+    // base itself must be 1024-byte aligned (128-byte swizzle atoms); if it is
+    // not, report it and leave before touching any barrier or tensor memory.
+    const uint32_t base = smem_u32(smem_raw);
+    if (base & 1023u) {
+        if (threadIdx.x == 0 && p.status) atomicOr(p.status, kErrSmemAlign);
+        return;
+    }
+    uint8_t* gbase = smem_raw;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::misc + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::misc);
     float* vec = reinterpret_cast<float*>(gbase + L::vec);
@@ -489,82 +501,79 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_bf16_f32(kBlockK, kBwdTile);
             constexpr uint32_t id_dk = idesc_bf16_f32(kBlockK, D, 0, 1);
-            constexpr uint32_t id_dq = idesc_bf16_f32(D, kBwdTile, 1, 1);
-            const uint32_t t_dk = tmem + 256;
-            auto issue_s = [&](int m) {
-                const int s = m % NST, buf = m & 1;
-                const uint32_t q1s = base + L::q + 2 * s * L::kQBytes;
-                const uint32_t d1 = tmem + buf * 128, d2 = d1 + 64;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t ko = (kk >> 2) * kBlockK * 128 + (kk & 3) * 32;
-                    const uint32_t qo = (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32;
-                    tc_mma_bf16(d1, smem_desc_k128(base + L::k1 + ko), smem_desc_k128(q1s + qo), id_s, kk > 0);
-                }
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t ko = (kk >> 2) * kBlockK * 128 + (kk & 3) * 32;
-                    const uint32_t qo = (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32;
-                    tc_mma_bf16(d2, smem_desc_k128(base + L::k2 + ko), smem_desc_k128(q1s + L::kQBytes + qo), id_s,
-                                kk > 0);
-                }
-                tc_commit(base + L::bar_sfull + 8 * buf);
-            };
+            constexpr uint32_t id_dq = idesc_bf16_f32(D, 2 * kBwdTile, 1, 1);
+            const uint32_t t_k = tmem, t_s = tmem + 128, t_dk = tmem + 256, t_dq = tmem + 384;
             int issued = 0;
             bool started = false;
             // test aid: a wait on a barrier that nothing arrives on before the end
             const bool stalled = p.inject_stall && blockIdx.x == 0 &&
                                  !mbar_wait(base + L::bar_done, 0, wc, kErrWaitOther);
-            bool ok = !stalled && mbar_wait(base + L::bar_k, 0, wc, kErrWaitK) &&
-                      mbar_wait(base + L::bar_qfull, 0, wc, kErrWaitQ);
+            bool ok = !stalled && mbar_wait(base + L::bar_k, 0, wc, kErrWaitK);
             if (ok) {
                 tc_fence_after();
-                issue_s(0);
+                // the CTA's key tiles become the A operand of every score MMA
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t ko = (kk >> 2) * kBlockK * 128 + (kk & 3) * 32;
+                    tc_cp_128x256b(t_k + kk * 8, smem_desc_k128(base + L::k1 + ko));
+                    tc_cp_128x256b(t_k + D / 2 + kk * 8, smem_desc_k128(base + L::k2 + ko));
+                }
                 started = true;
-                for (int m = 0; m < n_tiles; ++m) {
-                    if (m + 1 < n_tiles) {
-                        const int n1 = m + 1;
-                        if (!mbar_wait(base + L::bar_qfull + 8 * (n1 % NST), (n1 / NST) & 1, wc, kErrWaitQ)) break;
-                        if (!mbar_wait(base + L::bar_sempty + 8 * (n1 & 1), ((n1 >> 1) & 1) ^ 1, wc, kErrWaitS))
+                // iteration m issues the scores of tile m, then the gradient MMAs of tile m - 1
+                for (int m = 0; m <= n_tiles; ++m) {
+                    if (m < n_tiles) {
+                        const int s = m % NST;
+                        if (!mbar_wait(base + L::bar_qfull + 8 * s, (m / NST) & 1, wc, kErrWaitQ)) break;
+                        if (!mbar_wait(base + L::bar_sempty, (m & 1) ^ 1, wc, kErrWaitS)) break;
+                        tc_fence_after();
+                        const uint32_t q1s = base + L::q + 2 * s * L::kQBytes;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t qo = (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32;
+                            tc_mma_bf16_ta(t_s, t_k + kk * 8, smem_desc_k128(q1s + qo), id_s, kk > 0);
+                        }
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t qo = (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32;
+                            tc_mma_bf16_ta(t_s + 64, t_k + D / 2 + kk * 8, smem_desc_k128(q1s + L::kQBytes + qo),
+                                           id_s, kk > 0);
+                        }
+                        tc_commit(base + L::bar_sfull);
+                    }
+                    if (m > 0) {
+                        const int mm = m - 1, s = mm % NST, dsb = mm % L::kNumDs;
+                        if (!mbar_wait(base + L::bar_dsfull + 8 * dsb, (mm / L::kNumDs) & 1, wc, kErrWaitOther))
                             break;
                         tc_fence_after();
-                        issue_s(n1);
-                    }
-                    const int s = m % NST, buf = m & 1;
-                    const int dsb = m % L::kNumDs;
-                    if (!mbar_wait(base + L::bar_dsfull + 8 * dsb, (m / L::kNumDs) & 1, wc, kErrWaitOther)) break;
-                    tc_fence_after();
-                    const uint32_t dss = base + L::ds + 2 * dsb * L::kDsBytes;
-                    const uint32_t qts = base + L::q + 2 * s * L::kQBytes + qt_off;
-                    // dK += dS^T Q_t : A = dS^T (K-major over queries), B = Q_t (MN-major); dS = hi + lo
-#pragma unroll
-                    for (int part = 0; part < 2; ++part)
-#pragma unroll
-                        for (int kk = 0; kk < kBwdTile / 16; ++kk)
-                            tc_mma_bf16(t_dk, smem_desc_k128(dss + part * L::kDsBytes + kk * 32),
-                                        smem_desc_mn128(qts + kk * 16 * 128, kBwdTile * 128), id_dk,
-                                        (m | kk | part) != 0);
-                    if (FUSED) {
-                        // dQ^T = K_t^T dS^T : A = K_t (MN-major), B = dS^T (MN-major), K = 128 keys
-                        if (!mbar_wait(base + L::bar_dqempty + 8 * buf, ((m >> 1) & 1) ^ 1, wc, kErrWaitOther)) break;
-                        tc_fence_after();
-                        const uint32_t t_dq = tmem + 384 + buf * kBwdTile;
+                        const uint32_t dss = base + L::ds + 2 * dsb * L::kDsBytes;
+                        const uint32_t qts = base + L::q + 2 * s * L::kQBytes + qt_off;
+                        // dK += dS^T Q_t : A = dS^T (K-major over queries), B = Q_t (MN-major); dS = hi + lo
 #pragma unroll
                         for (int part = 0; part < 2; ++part)
 #pragma unroll
+                            for (int kk = 0; kk < kBwdTile / 16; ++kk)
+                                tc_mma_bf16(t_dk, smem_desc_k128(dss + part * L::kDsBytes + kk * 32),
+                                            smem_desc_mn128(qts + kk * 16 * 128, kBwdTile * 128), id_dk,
+                                            (mm | kk | part) != 0);
+                        if (FUSED) {
+                            // [dQ^T_hi | dQ^T_lo] = K_t^T [dS^T_hi | dS^T_lo]: A = K_t (MN-major), B = the
+                            // hi and lo tiles as two 64-query atoms of one N = 128 operand, K = 128 keys
+                            if (!mbar_wait(base + L::bar_dqempty, (mm & 1) ^ 1, wc, kErrWaitOther)) break;
+                            tc_fence_after();
+#pragma unroll
                             for (int kk = 0; kk < kBlockK / 16; ++kk)
                                 tc_mma_bf16(t_dq, smem_desc_mn128(kt_tile + kk * 16 * 128, kBlockK * 128),
-                                            smem_desc_mn128(dss + part * L::kDsBytes + kk * 16 * 128, kBlockK * 128),
-                                            id_dq, (kk | part) != 0);
-                        tc_commit(base + L::bar_dqfull + 8 * buf);
+                                            smem_desc_mn128(dss + kk * 16 * 128, L::kDsBytes), id_dq, kk > 0);
+                            tc_commit(base + L::bar_dqfull);
+                        }
+                        tc_commit(base + L::bar_dsempty + 8 * dsb);
+                        tc_commit(base + L::bar_qempty + 8 * s);
+                        ++issued;
                     }
-                    tc_commit(base + L::bar_dsempty + 8 * dsb);
-                    tc_commit(base + L::bar_qempty + 8 * s);
-                    ++issued;
                 }
                 if (issued == n_tiles) tc_commit(base + L::bar_done);
             }
-            if (*abort_flag && started) {  // let the issued MMAs retire before TMEM is freed
+            if (*abort_flag && started) {  // let the issued copies and MMAs retire before TMEM is freed
                 tc_commit(base + L::bar_done);
                 drain_wait_b(base + L::bar_done, 0, kDrainNs);
             }
@@ -582,15 +591,15 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
         const bool key_ok = j < p.Nk;
         bool ok = true;
         for (int m = 0; m < n_tiles; ++m) {
-            const int s = m % NST, buf = m & 1;
-            if (!wait_all(base + L::bar_sfull + 8 * buf, (m >> 1) & 1, wc, kErrWaitS) ||
+            const int s = m % NST;
+            if (!wait_all(base + L::bar_sfull, m & 1, wc, kErrWaitS) ||
                 !wait_all(base + L::bar_qfull + 8 * s, (m / NST) & 1, wc, kErrWaitQ)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const int r0 = (m_start + m) * kBwdTile + wg * 32;  // first query row of this chunk
-            const uint32_t t1 = tl + buf * 128 + wg * 32, t2 = t1 + 64;
+            const uint32_t t1 = tl + 128 + wg * 32, t2 = t1 + 64;
             const int dsb = m % L::kNumDs;
             const uint32_t dss = base + L::ds + 2 * dsb * L::kDsBytes;
             float z1[32], z2[32];
@@ -598,7 +607,7 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
             tmem_ld32(t2, z2);
             tc_wait_ld();
             tc_fence_before();
-            mbar_arrive(base + L::bar_sempty + 8 * buf);
+            mbar_arrive(base + L::bar_sempty);  // the next score tile may overwrite S now
             // per-query constants of this chunk: 128-bit broadcast loads
             const float4* v4 = reinterpret_cast<const float4*>(vec + s * 3 * kBwdTile + wg * 32);
             float dsv[32];
@@ -646,30 +655,57 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
             }
         }
     } else if (FUSED) {
-        // ------------------------------------------------ dQ^T -> atomics into dQ
+        // ------------------------------------------------ dQ^T -> bulk L2 reduction into dQ
+        // Each tile's 64 x d float32 block of dQ is staged in shared memory as
+        // 64 contiguous rows (the non-trainable key tile's space: that tile
+        // only fed the copy into tensor memory) and added to global dQ with
+        // one bulk reduce-add.
         const int wq = warp & 3;
         const int f = wq * 32 + lane;  // feature = TMEM lane
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+        const uint32_t stage = base + (SETTING == 1 ? L::k1 : L::k2);
+        const bool leader = warp == 10 && lane == 0;
         for (int m = 0; m < n_tiles; ++m) {
-            const int buf = m & 1;
-            if (!wait_all(base + L::bar_dqfull + 8 * buf, (m >> 1) & 1, wc, kErrWaitOther)) break;
+            // the four epilogue warps decide together, so none is left at a named barrier
+            if (!bar_sync_and(3, 128, wait_all(base + L::bar_dqfull, m & 1, wc, kErrWaitOther))) break;
             tc_fence_after();
             float v0[32], v1[32];
-            tmem_ld32(tl + 384 + buf * kBwdTile, v0);
-            tmem_ld32(tl + 384 + buf * kBwdTile + 32, v1);
-            tc_wait_ld();
+            {
+                float lo[32];
+                tmem_ld32(tl + 384, v0);  // hi half, query rows 0-31
+                tmem_ld32(tl + 448, lo);  // lo half, query rows 0-31
+                tc_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v0[e] += lo[e];
+                tmem_ld32(tl + 416, v1);  // hi half, query rows 32-63
+                tmem_ld32(tl + 480, lo);  // lo half, query rows 32-63
+                tc_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v1[e] += lo[e];
+            }
             tc_fence_before();
-            mbar_arrive(base + L::bar_dqempty + 8 * buf);
+            mbar_arrive(base + L::bar_dqempty);
+            if (leader) bulk_wait_read_all();  // the previous tile's reduction has read the stage
+            asm volatile("bar.sync 2, 128;" ::: "memory");
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(stage + e * (D * 4) + f * 4), "f"(v0[e] * p.scale)
+                             : "memory");
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(stage + (e + 32) * (D * 4) + f * 4),
+                             "f"(v1[e] * p.scale)
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            asm volatile("bar.sync 2, 128;" ::: "memory");
             const int r0 = (m_start + m) * kBwdTile;
-            float* out = p.dQ + (static_cast<size_t>(bh) * p.Nq + r0) * D + f;
             const int nrow = min(kBwdTile, p.Nq - r0);
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-                if (e < nrow) red_add_f32(out + static_cast<size_t>(e) * D, v0[e] * p.scale);
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-                if (e + 32 < nrow) red_add_f32(out + static_cast<size_t>(e + 32) * D, v1[e] * p.scale);
+            if (leader && nrow > 0) {
+                bulk_reduce_add_f32(p.dQ + (static_cast<size_t>(bh) * p.Nq + r0) * D, stage,
+                                    static_cast<uint32_t>(nrow * D * 4));
+                bulk_commit();
+            }
         }
+        if (leader) bulk_wait_all();  // every reduction has landed before the CTA exits
     }
 
     tc_fence_before();
