@@ -129,6 +129,14 @@ def gpu_id(dev):
         return str(dev.index or 0)
 
 
+def config_for(w, world):
+    return {"workload": f"{w.name}: B={w.B} H={w.H} N_Q={w.Nq} N_K={w.Nk} d={w.d} "
+                        f"{'causal' if w.causal else 'non-causal'}, "
+                        + ("fwd only (Split-K decode) per step" if w.fwd_only else
+                           "fwd + bwd setting 1 + bwd setting 2 per step"),
+            "l2": "256 MB write between steps", "parallelism": f"heads-independent replicas x{world}"}
+
+
 def flush_l2(buf):
     buf.add_(1)  # a write larger than L2 between timed steps
 
@@ -155,18 +163,20 @@ def cpu_oracle_sample(w, budget_s=15.0):
         rows = rng.integers(0, w.Nq, size=n)
         t0 = time.perf_counter()
         oracle.fwd_rows(Q1n, K1n, Q2n, K2n, rows, causal=w.causal)
-        oracle.bwd_dq_rows(1, gn, Q1n, K1n, Q2n, K2n, rows, causal=w.causal)
-        oracle.bwd_dq_rows(2, gn, Q1n, K1n, Q2n, K2n, rows, causal=w.causal)
+        if not w.fwd_only:
+            oracle.bwd_dq_rows(1, gn, Q1n, K1n, Q2n, K2n, rows, causal=w.causal)
+            oracle.bwd_dq_rows(2, gn, Q1n, K1n, Q2n, K2n, rows, causal=w.causal)
         elapsed += time.perf_counter() - t0
         off = w.Nk - w.Nq
         done_pairs += int(sum(min(w.Nk, int(i) + off + 1) if w.causal else w.Nk for i in rows))
         nrows += n
     # algorithmic flops the GPU metric credits for these pairs: 4d (fwd) + 2 x 8d (bwd)
-    flops = 20 * w.d * done_pairs
+    per_pair = 4 if w.fwd_only else 20
+    flops = per_pair * w.d * done_pairs
     return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{nrows} random query rows of one head of {w.name} (N_Q={w.Nq} N_K={w.Nk} d={w.d}): "
-                      f"forward + dQ of both settings per row, {elapsed:.1f} s, float64, "
-                      f"{done_pairs} visible pairs; credited 20*d flops per pair",
+                      f"{'forward' if w.fwd_only else 'forward + dQ of both settings'} per row, "
+                      f"{elapsed:.1f} s, float64, {done_pairs} visible pairs; credited {per_pair}*d flops per pair",
             "seconds": elapsed}
 
 
@@ -324,12 +334,7 @@ def run_gpu(args):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws_, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) teacher, student +0.3 N(0,1))",
-            "config": {"workload": f"{w.name}: B={B} H={H} N_Q={Nq} N_K={Nk} d={d} "
-                                   f"{'causal' if w.causal else 'non-causal'}, "
-                                   + ("fwd only (Split-K decode) per step" if w.fwd_only else
-                                      "fwd + bwd setting 1 + bwd setting 2 per step"),
-                       "l2": "256 MB write between steps",
-                       "parallelism": f"heads-independent replicas x{ws_}"},
+            "config": config_for(w, ws_),
             "kernels": kernels, "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "device_error_word": status, "kl_mean": kl_mean,
             "peaks": {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"], "source": peak_src},
@@ -343,7 +348,7 @@ def run_reference(args):
     ws_, rank, _ = dist_env()
     if rank != 0:
         return None
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[args.workload]
     for _ in range(args.warmup):
         cpu_oracle_sample(w, budget_s=0.5)
     vals = []
@@ -351,10 +356,12 @@ def run_reference(args):
         vals.append(cpu_oracle_sample(w, budget_s=max(2.0, 30.0 / max(1, args.steps))))
     v = statistics.median(x["value"] for x in vals)
     last = vals[-1]
+    step_flops = (4 if w.fwd_only else 20) * w.d * w.visible_pairs() * w.B * w.H  # fwd 4d (+ 2 x 8d bwd)
     return {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": ws_, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64", "data": "synthetic", "config": {"workload": f"{WORKLOAD} (sampled rows on host cores)"},
+        "warmup": args.warmup, "ms_per_step": step_flops / (v * 1e12) * 1e3, "ms_per_step_kind": "extrapolated",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded N(0,1) teacher, student +0.3 N(0,1))", "config": config_for(w, ws_),
         "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
                          "sample": last["sample"]},
         "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
