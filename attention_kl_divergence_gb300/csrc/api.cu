@@ -79,7 +79,7 @@ streamkl_status plan_fwd(const streamkl_shape* s, int causal, const streamkl_opt
     int sms = 0;
     if ((st = device_sms(&sms)) != STREAMKL_OK) return st;
     const int64_t BH = int64_t(s->B) * s->H;
-    pl->decode = (s->Nq <= kDecodeMaxQ) && !causal;
+    pl->decode = s->Nq <= kDecodeMaxQ;
     pl->num_q_tiles = pl->decode ? 1 : (s->Nq + kBlockQ - 1) / kBlockQ;
     pl->num_k_tiles = (s->Nk + kBlockK - 1) / kBlockK;
     const int64_t units = BH * pl->num_q_tiles;

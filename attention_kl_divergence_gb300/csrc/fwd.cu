@@ -22,6 +22,10 @@ namespace streamkl {
 namespace {
 
 constexpr float kTau = 8.0f;  // lazy rescale: tolerate running maxima up to 2^8 stale
+// Update warpgroups of the tile kernel: each takes 128 / (32 * kFwdGroups)
+// 32-column chunks of every score tile and keeps its own running state per row.
+constexpr int kFwdGroups = 2;
+constexpr int kFwdThreads = 64 + 128 * kFwdGroups;
 // Bound of the waits that let in-flight TMA copies and MMAs retire before a CTA
 // exits (independent of the caller's wait limit).
 constexpr uint64_t kDrainNs = 200000000ull;
@@ -44,8 +48,8 @@ struct TileSmem {
     static constexpr int bar_sempty = bar_sfull + 16;
     static constexpr int bar_done = bar_sempty + 16;  // drain barrier of an aborted MMA issuer
     static constexpr int misc = bar_done + 8;     // tmem base (4 B), abort flag (4 B)
-    static constexpr int red = misc + 16;         // [5][128] floats: second warpgroup's row states
-    static constexpr int total = red + 5 * 128 * 4;
+    static constexpr int red = misc + 16;         // [groups - 1][5][128] floats: the other groups' row states
+    static constexpr int total = red + (kFwdGroups - 1) * 5 * 128 * 4;
     static constexpr int alloc = total + 1024;    // slack for 1024-byte alignment
 };
 
@@ -161,13 +165,13 @@ __device__ __forceinline__ void store_row(const FwdParams& p, size_t row, int sp
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Tile forward.  CTA = 10 warps: warp 0 issues TMA, warp 1 owns TMEM and
-// issues the MMAs, warps 2-9 run the online update (two warpgroups, one query
-// row per thread each, splitting the tile's columns).  TMEM: two buffers x
-// (S1 | S2), 128 columns each.
+// Tile forward.  Warp 0 issues TMA, warp 1 owns TMEM and issues the MMAs, the
+// remaining kFwdGroups warpgroups run the online update (one query row per
+// thread, each group taking its share of the tile's columns).  TMEM: two
+// buffers x (S1 | S2), 128 columns each.
 // ---------------------------------------------------------------------------
 template <int D, int NST>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(kFwdThreads, 1)
     fwd_tile_kernel(const __grid_constant__ CUtensorMap tQ1, const __grid_constant__ CUtensorMap tK1,
                     const __grid_constant__ CUtensorMap tQ2, const __grid_constant__ CUtensorMap tK2,
                     const FwdParams p) {
@@ -205,7 +209,7 @@ __global__ void __launch_bounds__(320, 1)
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(base + L::bar_sfull + 8 * s, 1);
-            mbar_init(base + L::bar_sempty + 8 * s, 256);
+            mbar_init(base + L::bar_sempty + 8 * s, 128 * kFwdGroups);
         }
         mbar_init(base + L::bar_done, 1);
         *abort_flag = 0;
@@ -296,10 +300,10 @@ __global__ void __launch_bounds__(320, 1)
         }
     } else {
         // ------------------------------------------------------------ online update
-        // Two warpgroups: warps 2-5 take columns 0-63 of every tile, warps 6-9
-        // columns 64-127, each with its own running state for its columns;
-        // the two states of a row are merged at the end (the same log-sum-exp
-        // merge as the Split-K combine).
+        // kFwdGroups warpgroups split every tile's 128 columns; each keeps its
+        // own running state per row, and the states of a row are merged at the
+        // end (the same log-sum-exp merge as the Split-K combine).
+        constexpr int kChunks = 4 / kFwdGroups;  // 32-column chunks per group and tile
         const int wg = (warp - 2) >> 2;
         const int wq = warp & 3;
         const int row = wq * 32 + lane;
@@ -320,13 +324,13 @@ __global__ void __launch_bounds__(320, 1)
             const int jrem = limit - (kt_begin + it) * kBlockK;  // last visible column of this tile
             const uint32_t t1 = tl + buf * 2 * kBlockK, t2 = t1 + kBlockK;
 #pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
-                const int ch = 2 * wg + cc;
+            for (int cc = 0; cc < kChunks; ++cc) {
+                const int ch = kChunks * wg + cc;
                 float z1[32], z2[32];
                 tmem_ld32(t1 + ch * 32, z1);
                 tmem_ld32(t2 + ch * 32, z2);
                 tc_wait_ld();
-                if (cc == 1) {
+                if (cc == kChunks - 1) {
                     tc_fence_before();
                     mbar_arrive(base + L::bar_sempty + 8 * buf);
                 }
@@ -338,17 +342,21 @@ __global__ void __launch_bounds__(320, 1)
             }
         }
         float* red = reinterpret_cast<float*>(gbase + L::red);
-        if (wg == 1) {
-            red[row] = st.m1;
-            red[128 + row] = st.l1;
-            red[256 + row] = st.acc;
-            red[384 + row] = st.m2;
-            red[512 + row] = st.l2;
+        if (wg > 0) {
+            float* r = red + (wg - 1) * 5 * 128;
+            r[row] = st.m1;
+            r[128 + row] = st.l1;
+            r[256 + row] = st.acc;
+            r[384 + row] = st.m2;
+            r[512 + row] = st.l2;
         }
-        asm volatile("bar.sync 1, 256;" ::: "memory");  // the eight update warps only
+        asm volatile("bar.sync 1, %0;" ::"r"(128 * kFwdGroups) : "memory");  // the update warps only
         if (wg == 0) {
-            const RowState o{red[row], red[128 + row], red[256 + row], red[384 + row], red[512 + row]};
-            merge_state(st, o, c);
+            for (int k = 0; k < kFwdGroups - 1; ++k) {
+                const float* r = red + k * 5 * 128;
+                const RowState o{r[row], r[128 + row], r[256 + row], r[384 + row], r[512 + row]};
+                merge_state(st, o, c);
+            }
             if (i < p.Nq) store_row(p, static_cast<size_t>(bh) * p.Nq + i, split, st, !ok || *abort_flag);
         }
     }
@@ -363,7 +371,7 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Decode forward, Nq <= 16, no mask.  S^T = K Q^T: M = 128 keys (TMEM lanes),
+// Decode forward, Nq <= 16 (causal or not).  S^T = K Q^T: M = 128 keys (TMEM lanes),
 // N = 16 query columns.  Each thread owns one key per step and keeps a running
 // state per query; the 128 states are merged at the end of the key range.
 // ---------------------------------------------------------------------------
@@ -531,10 +539,14 @@ __global__ void __launch_bounds__(192, 1)
             tc_wait_ld();
             tc_fence_before();
             mbar_arrive(base + L::bar_sempty + 8 * buf);
-            if ((kt_begin + it) * kBlockK + krow >= p.Nk) continue;  // key tail
+            const int j = (kt_begin + it) * kBlockK + krow;
+            if (j >= p.Nk) continue;  // key tail
+            // causal (bottom-right): query q sees key j iff j <= q + diag_off; keys up to
+            // diag_off are seen by every query
+            const int first_q = p.causal ? j - p.diag_off : 0;
 #pragma unroll
             for (int q = 0; q < NQ; ++q) {
-                if (q < nq) {
+                if (q < nq && q >= first_q) {
                     if (z1[q] > m1[q] + tau) {
                         const float a = ex2(c * (m1[q] - z1[q]));
                         l1[q] *= a;
@@ -633,12 +645,12 @@ cudaError_t launch_fwd_tile(int d, const CUtensorMap* maps, const FwdParams& p, 
         constexpr int NST = 2;
         auto k = fwd_tile_kernel<128, NST>;
         if ((e = ensure_smem(k, TileSmem<128, NST>::alloc)) != cudaSuccess) return e;
-        k<<<ctas, 320, TileSmem<128, NST>::alloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+        k<<<ctas, kFwdThreads, TileSmem<128, NST>::alloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
     } else {
         constexpr int NST = 4;
         auto k = fwd_tile_kernel<64, NST>;
         if ((e = ensure_smem(k, TileSmem<64, NST>::alloc)) != cudaSuccess) return e;
-        k<<<ctas, 320, TileSmem<64, NST>::alloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
+        k<<<ctas, kFwdThreads, TileSmem<64, NST>::alloc, stream>>>(maps[0], maps[1], maps[2], maps[3], p);
     }
     return cudaGetLastError();
 }

@@ -62,6 +62,9 @@ WORKLOADS = {
     "decode_q16_k128k": Workload("decode_q16_k128k", 4, 32, 16, 131072, 128, 0.3, False, seed=3, fwd_only=True),
     "decode_q1_k512k": Workload("decode_q1_k512k", 4, 32, 1, 524288, 128, 0.3, False, seed=3, fwd_only=True),
     "decode_q16_k512k": Workload("decode_q16_k512k", 4, 32, 16, 524288, 128, 0.3, False, seed=3, fwd_only=True),
+    # causal (bottom-right) Split-K: 16 new queries against a 128K-key prefix (chunked prefill)
+    "decode_causal_q16_k128k": Workload("decode_causal_q16_k128k", 4, 32, 16, 131072, 128, 0.3, True, seed=5,
+                                        fwd_only=True),
     # one batch of the 128K decode: small enough for a full ncu capture (2 GiB of keys)
     "decode_q1_k128k_b1": Workload("decode_q1_k128k_b1", 1, 32, 1, 131072, 128, 0.3, False, seed=3,
                                    fwd_only=True),

@@ -93,7 +93,7 @@ typedef struct {
 
 /* What a call will launch for a given shape (filled by the plan queries). */
 typedef struct {
-    int32_t path;       /* 0 = tile forward, 1 = decode (Nq <= 16) forward,
+    int32_t path;       /* 0 = tile forward, 1 = decode (Nq <= 16, causal or not) forward,
                            2 = fused backward, 3 = separate-kernel backward */
     int32_t num_splits; /* key splits of the forward (1 = no combine step)  */
     int32_t num_ctas;   /* CTAs of the main kernel                          */

@@ -139,3 +139,17 @@ def test_8k_causal_setting1_sampled():
 
 def test_8k_causal_setting2_sampled():
     check_sampled_grads(WORKLOADS["8k_causal"], 2)
+
+
+@pytest.mark.parametrize("setting", [1, 2])
+@pytest.mark.parametrize("mode", [FUSED, SPLIT])
+def test_bnhd_layout_views_backward(setting, mode):
+    """Strided [B, N, H, d] inputs give the same gradients (outputs stay [B, H, N, d])."""
+    B, H, N, d = 1, 2, 260, 128
+    base = make_qk(B, H, N, N, d, 0.4, seed=17, device=DEV)
+    views = [t.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3) for t in base]
+    g = torch.rand((B, H, N), device=DEV) + 0.5
+    dQ, dK = gpu_grads(setting, *views, g, True, mode)
+    rdQ, rdK = oracle.bwd(setting, g, *base, causal=True)
+    assert_grad(dQ, rdQ, "dQ (B N H d views)")
+    assert_grad(dK, rdK, "dK (B N H d views)")

@@ -100,16 +100,17 @@ def test_64k_noncausal_forward_and_both_settings():
         assert cos > 0.99999 and rel < 1e-2, (cos, rel)
 
 
-@pytest.mark.parametrize("name", ["decode_q1_k128k", "decode_q16_k128k", "decode_q1_k512k", "decode_q16_k512k"])
+@pytest.mark.parametrize("name", ["decode_q1_k128k", "decode_q16_k128k", "decode_q1_k512k", "decode_q16_k512k",
+                                  "decode_causal_q16_k128k"])
 def test_decode_split_k_all_rows_of_sampled_heads(name):
     w = WORKLOADS[name]
     inputs = make_workload(w, device=DEV)
-    plan = streamkl.fwd_plan(inputs[0], inputs[1])
+    plan = streamkl.fwd_plan(inputs[0], inputs[1], causal=w.causal)
     assert plan.path == streamkl.PATH_DECODE and plan.num_splits > 1
-    KL, L1, L2 = streamkl.kl_fwd(*inputs)
+    KL, L1, L2 = streamkl.kl_fwd(*inputs, causal=w.causal)
     torch.cuda.synchronize()
     for bh in (0, 37, 64, w.B * w.H - 1):
-        rKL, rL1, rL2 = oracle.fwd(*[head(t, bh) for t in inputs])
+        rKL, rL1, rL2 = oracle.fwd(*[head(t, bh) for t in inputs], causal=w.causal)
         assert_lse(L1.reshape(-1, w.Nq)[bh], rL1, f"LSE1 head {bh}")
         assert_lse(L2.reshape(-1, w.Nq)[bh], rL2, f"LSE2 head {bh}")
         assert_kl(KL.reshape(-1, w.Nq)[bh], rKL, f"KL head {bh}")

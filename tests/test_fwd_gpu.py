@@ -47,18 +47,40 @@ def test_tile_forward_shapes(B, H, Nq, Nk, d, causal, splits):
     run_and_check(Q1, K1, Q2, K2, causal, splits)
 
 
-@pytest.mark.parametrize("B,H,Nq,Nk,d,splits", [
-    (1, 2, 1, 1000, 64, 0),
-    (2, 2, 5, 4099, 128, 0),
-    (1, 3, 16, 2048, 128, 1),
-    (4, 2, 16, 130, 64, 7),
-    (1, 1, 3, 1, 128, 0),
+@pytest.mark.parametrize("B,H,Nq,Nk,d,splits,causal", [
+    (1, 2, 1, 1000, 64, 0, False),
+    (2, 2, 5, 4099, 128, 0, False),
+    (1, 3, 16, 2048, 128, 1, False),
+    (4, 2, 16, 130, 64, 7, False),
+    (1, 1, 3, 1, 128, 0, False),
+    # causal (bottom-right): decode steps and chunked prefill
+    (1, 2, 1, 1000, 64, 0, True),
+    (2, 2, 5, 4099, 128, 0, True),
+    (1, 3, 16, 2048, 128, 1, True),
+    (4, 2, 16, 130, 64, 7, True),
+    (1, 1, 16, 16, 128, 0, True),     # square: row i sees keys 0..i
+    (1, 2, 13, 300, 128, 3, True),
 ])
-def test_decode_forward_shapes(B, H, Nq, Nk, d, splits):
+def test_decode_forward_shapes(B, H, Nq, Nk, d, splits, causal):
     Q1, K1, Q2, K2 = make_qk(B, H, Nq, Nk, d, 0.3, seed=Nq * 7 + Nk, device=DEV)
-    plan = streamkl.fwd_plan(Q1, K1, causal=False, num_splits=splits)
+    plan = streamkl.fwd_plan(Q1, K1, causal=causal, num_splits=splits)
     assert plan.path == streamkl.PATH_DECODE
-    run_and_check(Q1, K1, Q2, K2, False, splits)
+    run_and_check(Q1, K1, Q2, K2, causal, splits)
+
+
+@pytest.mark.parametrize("Nq,Nk,causal", [(300, 300, True), (7, 5000, True), (200, 333, False)])
+def test_bnhd_layout_views(Nq, Nk, causal):
+    """[B, N, H, d] storage passed as permuted [B, H, N, d] views (strides only)."""
+    B, H, d = 2, 3, 128
+    base = make_qk(B, H, Nq, Nk, d, 0.4, seed=Nq + Nk, device=DEV)
+    views = [t.permute(0, 2, 1, 3).contiguous().permute(0, 2, 1, 3) for t in base]  # same values, B N H d memory
+    assert views[0].stride() == (Nq * H * d, d, H * d, 1)
+    KL, L1, L2 = streamkl.kl_fwd(*views, causal=causal)
+    torch.cuda.synchronize()
+    rKL, rL1, rL2 = oracle.fwd(*base, causal=causal)
+    assert_lse(L1, rL1, "LSE1")
+    assert_lse(L2, rL2, "LSE2")
+    assert_kl(KL, rKL)
 
 
 def test_identical_inputs_give_zero_kl():
