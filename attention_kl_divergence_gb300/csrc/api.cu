@@ -33,8 +33,11 @@ streamkl_status check_shape(const streamkl_shape* s, int causal) {
         if (v < 1 || (v % 8) != 0 || v > (int64_t(1) << 38)) return STREAMKL_ERR_INVALID_ARG;
     if (s->q_stride_n < s->d || s->k_stride_n < s->d) return STREAMKL_ERR_INVALID_ARG;
     if (int64_t(s->B) * s->H > (int64_t(1) << 24)) return STREAMKL_ERR_UNSUPPORTED;
+    if (s->H_kv < 0 || (s->H_kv > 0 && s->H % s->H_kv != 0)) return STREAMKL_ERR_INVALID_ARG;
     return STREAMKL_OK;
 }
+
+int kv_heads(const streamkl_shape* s) { return s->H_kv > 0 ? s->H_kv : s->H; }
 
 streamkl_status device_sms(int* sms) {
     int dev = 0;
@@ -127,7 +130,7 @@ streamkl_status plan_bwd(const streamkl_shape* s, int setting, int causal, const
         pl->fused = s->d == 128;
     else
         pl->fused = mode == 1;
-    const int64_t ctas_kv = BH * ((s->Nk + kBlockK - 1) / kBlockK);
+    const int64_t ctas_kv = int64_t(s->B) * kv_heads(s) * ((s->Nk + kBlockK - 1) / kBlockK);
     const int64_t ctas_q = BH * ((s->Nq + kBlockQ - 1) / kBlockQ);
     if (ctas_kv > INT32_MAX || ctas_q > INT32_MAX) return STREAMKL_ERR_UNSUPPORTED;
     pl->ctas_kv = static_cast<int>(ctas_kv);
@@ -159,7 +162,7 @@ bool make_map(CUtensorMap* m, const void* ptr, const streamkl_shape* s, bool is_
     const int64_t sb = is_q ? s->q_stride_b : s->k_stride_b;
     const int64_t sh = is_q ? s->q_stride_h : s->k_stride_h;
     const int64_t sn = is_q ? s->q_stride_n : s->k_stride_n;
-    cuuint64_t dims[4] = {cuuint64_t(s->d), cuuint64_t(N), cuuint64_t(s->H), cuuint64_t(s->B)};
+    cuuint64_t dims[4] = {cuuint64_t(s->d), cuuint64_t(N), cuuint64_t(is_q ? s->H : kv_heads(s)), cuuint64_t(s->B)};
     cuuint64_t strides[3] = {cuuint64_t(sn * 2), cuuint64_t(sh * 2), cuuint64_t(sb * 2)};
     cuuint32_t box[4] = {cuuint32_t(kSwizzleCols), cuuint32_t(box_rows), 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
@@ -245,6 +248,7 @@ streamkl_status streamkl_fwd(const streamkl_shape* shape, const void* Q1, const 
     p.num_splits = pl.num_splits;
     p.causal = causal ? 1 : 0;
     p.diag_off = shape->Nk - shape->Nq;
+    p.kv_group = shape->H / kv_heads(shape);
     p.scale = sc;
     p.scale_log2e = sc * 1.4426950408889634f;
     p.KL = KL;
@@ -315,6 +319,8 @@ streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const flo
     p.Nk = shape->Nk;
     p.causal = causal ? 1 : 0;
     p.diag_off = shape->Nk - shape->Nq;
+    p.H_kv = kv_heads(shape);
+    p.kv_group = shape->H / p.H_kv;
     p.scale = sc;
     p.scale_log2e = sc * 1.4426950408889634f;
     p.g = g;

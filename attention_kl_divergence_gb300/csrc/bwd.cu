@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(320, 1)
     const int qi = blockIdx.x - bh * p.num_q_tiles;
     const int qt = p.causal ? (p.num_q_tiles - 1 - qi) : qi;
     const int b = bh / p.H, h = bh - b * p.H;
+    const int hk = h / p.kv_group;  // key head (shared by kv_group query heads)
     const int q0 = qt * kBlockQ;
     const int q_last = min(q0 + kBlockQ, p.Nq) - 1;
     const int n_tiles = p.causal ? min(p.num_k_tiles, (q_last + p.diag_off) / kBwdTile + 1) : p.num_k_tiles;
@@ -194,8 +195,8 @@ __global__ void __launch_bounds__(320, 1)
                 const uint32_t k1s = base + L::k + 2 * s * L::kKBytes, k2s = k1s + L::kKBytes;
 #pragma unroll
                 for (int c = 0; c < D / kSwizzleCols; ++c) {
-                    tma_load_4d_hint(k1s + c * kBwdTile * 128, &tK1, fb, c * kSwizzleCols, k0, h, b, keep);
-                    tma_load_4d_hint(k2s + c * kBwdTile * 128, &tK2, fb, c * kSwizzleCols, k0, h, b, keep);
+                    tma_load_4d_hint(k1s + c * kBwdTile * 128, &tK1, fb, c * kSwizzleCols, k0, hk, b, keep);
+                    tma_load_4d_hint(k2s + c * kBwdTile * 128, &tK2, fb, c * kSwizzleCols, k0, hk, b, keep);
                 }
             }
             drain_wait_b(base + L::bar_q, 0, kDrainNs);  // the query tiles' copies have landed
@@ -410,13 +411,19 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
 
     // head-major: resident CTAs share one head's query tiles through L2; key
     // tile 0 sees the most query rows under a causal mask and comes first
-    const int bh = blockIdx.x / p.num_k_tiles;
-    const int nt = blockIdx.x - bh * p.num_k_tiles;
-    const int b = bh / p.H, h = bh - b * p.H;
+    // (a key head serves kv_group query heads: the CTA visits every query tile of each of them,
+    // so dK sums the group's gradients without a second pass)
+    const int bkv = blockIdx.x / p.num_k_tiles;  // flat (batch, key head)
+    const int nt = blockIdx.x - bkv * p.num_k_tiles;
+    const int b = bkv / p.H_kv, hk = bkv - b * p.H_kv;
     const int n0 = nt * kBlockK;
     // first 64-row query tile with a row that sees key n0 (row i sees keys j <= i + diag_off)
     const int m_start = p.causal ? max(0, (n0 - p.diag_off) / kBwdTile) : 0;
-    const int n_tiles = p.num_q_tiles - m_start;
+    const int per_head = p.num_q_tiles - m_start;  // query tiles of one query head that see this key tile
+    const int n_tiles = per_head * p.kv_group;
+    // iteration m -> (query head, query tile)
+    auto qhead = [&](int m) { return hk * p.kv_group + m / per_head; };
+    auto qtile = [&](int m) { return m_start + m % per_head; };
     const uint32_t kt_tile = base + (SETTING == 1 ? L::k2 : L::k1);  // trainable keys
     const uint32_t qt_off = SETTING == 1 ? L::kQBytes : 0;           // trainable queries within a stage
 
@@ -456,8 +463,8 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
             mbar_arrive_expect_tx(base + L::bar_k, 2 * L::kKBytes);
 #pragma unroll
             for (int c = 0; c < D / kSwizzleCols; ++c) {
-                tma_load_4d(base + L::k1 + c * kBlockK * 128, &tK1, base + L::bar_k, c * kSwizzleCols, n0, h, b);
-                tma_load_4d(base + L::k2 + c * kBlockK * 128, &tK2, base + L::bar_k, c * kSwizzleCols, n0, h, b);
+                tma_load_4d(base + L::k1 + c * kBlockK * 128, &tK1, base + L::bar_k, c * kSwizzleCols, n0, hk, b);
+                tma_load_4d(base + L::k2 + c * kBlockK * 128, &tK2, base + L::bar_k, c * kSwizzleCols, n0, hk, b);
             }
         }
         const uint64_t keep = policy_evict_last();
@@ -465,7 +472,8 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
         for (; m < n_tiles; ++m) {
             const int s = m % NST;
             if (!wait_all(base + L::bar_qempty + 8 * s, ((m / NST) & 1) ^ 1, wc, kErrWaitOther)) break;
-            const int r0 = (m_start + m) * kBwdTile;
+            const int r0 = qtile(m) * kBwdTile;
+            const int h = qhead(m);
             const uint32_t fb = base + L::bar_qfull + 8 * s;
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, 2 * L::kQBytes);
@@ -482,7 +490,7 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
                 const int r = lane + 32 * k;
                 const int i = r0 + r;
                 float la, xb, g;
-                row_constants<SETTING>(p, static_cast<size_t>(bh) * p.Nq + i, i < p.Nq, la, xb, g);
+                row_constants<SETTING>(p, (static_cast<size_t>(b) * p.H + h) * p.Nq + i, i < p.Nq, la, xb, g);
                 v[r] = la;
                 v[kBwdTile + r] = xb;
                 v[2 * kBwdTile + r] = g;
@@ -598,7 +606,7 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
                 break;
             }
             tc_fence_after();
-            const int r0 = (m_start + m) * kBwdTile + wg * 32;  // first query row of this chunk
+            const int r0 = qtile(m) * kBwdTile + wg * 32;  // first query row of this chunk
             const uint32_t t1 = tl + 128 + wg * 32, t2 = t1 + 64;
             const int dsb = m % L::kNumDs;
             const uint32_t dss = base + L::ds + 2 * dsb * L::kDsBytes;
@@ -640,7 +648,7 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
         // epilogue: dK row = scale * accumulator; each warpgroup writes half the columns
         if (ok && wait_all(base + L::bar_done, 0, wc, kErrWaitOther)) {
             tc_fence_after();
-            float* out = p.dK + (static_cast<size_t>(bh) * p.Nk + j) * D;
+            float* out = p.dK + (static_cast<size_t>(bkv) * p.Nk + j) * D;
 #pragma unroll 1
             for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 32) {
                 float v[32];
@@ -697,10 +705,10 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
             }
             fence_proxy_async_smem();
             asm volatile("bar.sync 2, 128;" ::: "memory");
-            const int r0 = (m_start + m) * kBwdTile;
+            const int r0 = qtile(m) * kBwdTile;
             const int nrow = min(kBwdTile, p.Nq - r0);
             if (leader && nrow > 0) {
-                bulk_reduce_add_f32(p.dQ + (static_cast<size_t>(bh) * p.Nq + r0) * D, stage,
+                bulk_reduce_add_f32(p.dQ + ((static_cast<size_t>(b) * p.H + qhead(m)) * p.Nq + r0) * D, stage,
                                     static_cast<uint32_t>(nrow * D * 4));
                 bulk_commit();
             }

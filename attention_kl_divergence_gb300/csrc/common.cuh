@@ -30,6 +30,7 @@ struct FwdParams {
     int num_splits;      // key-range splits per query tile (1 = write final outputs)
     int causal;          // bottom-right causal mask
     int diag_off;        // Nk - Nq
+    int kv_group;        // query heads per key head (1 = no sharing)
     float scale;         // softmax scale
     float scale_log2e;   // scale * log2(e): raw dot product -> base-2 exponent
     float* KL;           // [B*H*Nq]
@@ -48,6 +49,8 @@ struct BwdParams {
     int num_k_tiles;     // bwd_q: 64-key tiles;  bwd_kv: 128-key tiles
     int causal;
     int diag_off;        // Nk - Nq
+    int H_kv;            // key heads
+    int kv_group;        // query heads per key head
     float scale;
     float scale_log2e;
     const float* g;      // [B*H*Nq] upstream gradient dL/dKL
@@ -55,7 +58,7 @@ struct BwdParams {
     const float* LSE1;
     const float* LSE2;
     float* dQ;           // [B*H*Nq, d]
-    float* dK;           // [B*H*Nk, d]
+    float* dK;           // [B*H_kv*Nk, d]
     unsigned int* status;
     unsigned long long wait_ns;
     int inject_stall;

@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int split = rem - qi * p.num_splits;
     const int qt = p.causal ? (p.num_q_tiles - 1 - qi) : qi;
     const int b = bh / p.H, h = bh - b * p.H;
+    const int hk = h / p.kv_group;  // key head (shared by kv_group query heads)
     const int q0 = qt * kBlockQ;
     const int q_last = min(q0 + kBlockQ, p.Nq) - 1;
     const int kt_total = p.causal ? min(p.num_k_tiles, (q_last + p.diag_off) / kBlockK + 1) : p.num_k_tiles;
@@ -247,8 +248,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 const uint32_t k1s = base + L::k + 2 * s * L::kKBytes, k2s = k1s + L::kKBytes;
 #pragma unroll
                 for (int c = 0; c < D / kSwizzleCols; ++c) {
-                    tma_load_4d_hint(k1s + c * kBlockK * 128, &tK1, fb, c * kSwizzleCols, k0, h, b, keep);
-                    tma_load_4d_hint(k2s + c * kBlockK * 128, &tK2, fb, c * kSwizzleCols, k0, h, b, keep);
+                    tma_load_4d_hint(k1s + c * kBlockK * 128, &tK1, fb, c * kSwizzleCols, k0, hk, b, keep);
+                    tma_load_4d_hint(k2s + c * kBlockK * 128, &tK2, fb, c * kSwizzleCols, k0, hk, b, keep);
                 }
             }
             // drain: every issued copy has landed and every stage was released
@@ -413,6 +414,7 @@ __global__ void __launch_bounds__(192, 1)
     const int bh = blockIdx.x / p.num_splits;
     const int split = blockIdx.x - bh * p.num_splits;
     const int b = bh / p.H, h = bh - b * p.H;
+    const int hk = h / p.kv_group;  // key head (shared by kv_group query heads)
     const int per_split = (p.num_k_tiles + p.num_splits - 1) / p.num_splits;
     const int kt_begin = split * per_split;
     const int n_tiles = max(0, min(p.num_k_tiles, kt_begin + per_split) - kt_begin);
@@ -462,8 +464,8 @@ __global__ void __launch_bounds__(192, 1)
                 const uint32_t k1s = base + L::k + 2 * s * L::kKBytes, k2s = k1s + L::kKBytes;
 #pragma unroll
                 for (int c = 0; c < D / kSwizzleCols; ++c) {
-                    tma_load_4d_hint(k1s + c * kBlockK * 128, &tK1, fb, c * kSwizzleCols, k0, h, b, stream_once);
-                    tma_load_4d_hint(k2s + c * kBlockK * 128, &tK2, fb, c * kSwizzleCols, k0, h, b, stream_once);
+                    tma_load_4d_hint(k1s + c * kBlockK * 128, &tK1, fb, c * kSwizzleCols, k0, hk, b, stream_once);
+                    tma_load_4d_hint(k2s + c * kBlockK * 128, &tK2, fb, c * kSwizzleCols, k0, hk, b, stream_once);
                 }
             }
             drain_wait(base + L::bar_q, 0, kDrainNs);  // the query tiles' copies have landed

@@ -30,7 +30,7 @@ class Shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("Nq", ctypes.c_int32), ("Nk", ctypes.c_int32),
                 ("d", ctypes.c_int32), ("q_stride_b", ctypes.c_int64), ("q_stride_h", ctypes.c_int64),
                 ("q_stride_n", ctypes.c_int64), ("k_stride_b", ctypes.c_int64), ("k_stride_h", ctypes.c_int64),
-                ("k_stride_n", ctypes.c_int64)]
+                ("k_stride_n", ctypes.c_int64), ("H_kv", ctypes.c_int32)]
 
 
 class Options(ctypes.Structure):
@@ -113,7 +113,7 @@ def make_shape(Q1, K1) -> Shape:
     B, H, Nq, d = Q1.shape
     Nk = K1.shape[2]
     qs, ks = Q1.stride(), K1.stride()
-    return Shape(B, H, Nq, Nk, d, qs[0], qs[1], qs[2], ks[0], ks[1], ks[2])
+    return Shape(B, H, Nq, Nk, d, qs[0], qs[1], qs[2], ks[0], ks[1], ks[2], K1.shape[1])
 
 
 def _check_qk(Q1, K1, Q2, K2):
@@ -126,8 +126,10 @@ def _check_qk(Q1, K1, Q2, K2):
             raise ValueError(f"{name} must be [B, H, N, d] with d contiguous")
     if Q1.shape != Q2.shape or K1.shape != K2.shape or Q1.stride() != Q2.stride() or K1.stride() != K2.stride():
         raise ValueError("teacher and student tensors must have equal shapes and strides")
-    if Q1.shape[0] != K1.shape[0] or Q1.shape[1] != K1.shape[1] or Q1.shape[3] != K1.shape[3]:
-        raise ValueError("Q and K must share B, H and d")
+    if Q1.shape[0] != K1.shape[0] or Q1.shape[3] != K1.shape[3]:
+        raise ValueError("Q and K must share B and d")
+    if Q1.shape[1] % K1.shape[1] != 0:
+        raise ValueError("the key head count must divide the query head count")
 
 
 def _opts(num_splits=0, bwd_mode=0, wait_limit_ns=0, debug_flags=0):
@@ -179,7 +181,9 @@ def kl_fwd(Q1, K1, Q2, K2, causal=False, scale=None, num_splits=0, workspace=Non
 
 def kl_bwd(setting, g, Q1, K1, Q2, K2, KL, LSE1, LSE2, causal=False, scale=None, mode=BWD_AUTO, workspace=None,
            out=None, wait_limit_ns=0, debug_flags=0):
-    """(dQ, dK) float32 of the trainable side: setting 1 -> (Q2, K2), 2 -> (Q1, K1)."""
+    """(dQ, dK) float32 of the trainable side: setting 1 -> (Q2, K2), 2 -> (Q1, K1).
+    With keys shared by groups of query heads (K has fewer heads than Q), dK
+    has K's head count and sums the gradients of each group."""
     _check_qk(Q1, K1, Q2, K2)
     lib = load()
     shape = make_shape(Q1, K1)
@@ -194,7 +198,7 @@ def kl_bwd(setting, g, Q1, K1, Q2, K2, KL, LSE1, LSE2, causal=False, scale=None,
             raise ValueError(f"{name} must be contiguous float32 [B, H, Nq]")
     if out is None:
         out = (torch.empty((B, H, Nq, d), dtype=torch.float32, device=Q1.device),
-               torch.empty((B, H, Nk, d), dtype=torch.float32, device=Q1.device))
+               torch.empty((B, K1.shape[1], Nk, d), dtype=torch.float32, device=Q1.device))
     if workspace is None or workspace.numel() < plan.workspace_bytes:
         workspace = new_workspace(plan.workspace_bytes, Q1.device)
     dQ, dK = out

@@ -19,12 +19,14 @@
  *
  * Conventions shared by every entry point
  *  - Q1, K1, Q2, K2 are bf16 device tensors laid out [B, H, N, d] with d
- *    contiguous; the element strides of the B, H and N axes are given in
+ *    contiguous (K1, K2 have H_kv heads when keys are shared across a group
+ *    of query heads); the element strides of the B, H and N axes are given in
  *    streamkl_shape and must be multiples of 8 elements (16 bytes).  Q1 and
  *    Q2 share one set of strides, K1 and K2 another.  Base pointers must be
  *    16-byte aligned.  d must be 64 or 128.
  *  - KL, LSE1, LSE2 and g are float32 [B, H, Nq], contiguous.  dQ is float32
- *    [B, H, Nq, d] and dK float32 [B, H, Nk, d], contiguous.
+ *    [B, H, Nq, d] and dK float32 [B, H_kv, Nk, d], contiguous; with shared
+ *    keys dK sums the gradients of every query head of the group.
  *  - Logarithms are natural.  LSE_t[i] = log sum_j exp(S_t[i,j]) includes the
  *    softmax scale.
  *  - causal != 0 aligns the mask bottom-right: row i sees keys
@@ -73,6 +75,8 @@ typedef struct {
     int32_t B, H, Nq, Nk, d;
     int64_t q_stride_b, q_stride_h, q_stride_n; /* element strides of Q1 and Q2 */
     int64_t k_stride_b, k_stride_h, k_stride_n; /* element strides of K1 and K2 */
+    int32_t H_kv; /* key heads: 0 (or H) = one per query head; otherwise H_kv divides H and
+                     query head h uses key head h / (H / H_kv) (keys shared by a group) */
 } streamkl_shape;
 
 /* Optional knobs; pass NULL for the defaults. */

@@ -37,7 +37,7 @@ def _shape(**kw):
     s = dict(B=1, H=2, Nq=256, Nk=256, d=64)
     s.update(kw)
     d, Nq, Nk, H = s["d"], s["Nq"], s["Nk"], s["H"]
-    return sk.Shape(s["B"], H, Nq, Nk, d, H * Nq * d, Nq * d, d, H * Nk * d, Nk * d, d)
+    return sk.Shape(s["B"], H, Nq, Nk, d, H * Nq * d, Nq * d, d, H * Nk * d, Nk * d, d, s.get("H_kv", 0))
 
 
 def _fwd(shape, ptrs=(256,) * 7, ws=256, ws_bytes=4096, causal=0):
@@ -56,6 +56,8 @@ def test_fwd_rejects_bad_shapes_without_device():
     bad = _shape()
     bad.q_stride_n = 60  # not a multiple of 8 elements
     assert _fwd(bad) == sk.ERR_INVALID_ARG
+    assert _fwd(_shape(H=6, H_kv=4)) == sk.ERR_INVALID_ARG  # key heads must divide query heads
+    assert _fwd(_shape(H=6, H_kv=-1)) == sk.ERR_INVALID_ARG
 
 
 def test_fwd_rejects_bad_pointers_without_device():
