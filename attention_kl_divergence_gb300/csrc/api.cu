@@ -77,7 +77,8 @@ struct FwdPlan {
 streamkl_status plan_fwd(const streamkl_shape* s, int causal, const streamkl_options* opt, FwdPlan* pl) {
     streamkl_status st = check_shape(s, causal);
     if (st != STREAMKL_OK) return st;
-    if (opt && (opt->num_splits < 0 || opt->reserved != 0 || (opt->debug_flags & ~STREAMKL_DEBUG_INJECT_STALL)))
+    if (opt && (opt->num_splits < 0 || (opt->grad_bf16 != 0 && opt->grad_bf16 != 1) ||
+                (opt->debug_flags & ~STREAMKL_DEBUG_INJECT_STALL)))
         return STREAMKL_ERR_INVALID_ARG;
     int sms = 0;
     if ((st = device_sms(&sms)) != STREAMKL_OK) return st;
@@ -103,6 +104,7 @@ streamkl_status plan_fwd(const streamkl_shape* s, int causal, const streamkl_opt
 
 struct BwdPlan {
     bool fused;
+    bool bf16;
     int ctas_q;
     int ctas_kv;
     size_t ws_bytes;
@@ -121,7 +123,8 @@ streamkl_status plan_bwd(const streamkl_shape* s, int setting, int causal, const
     if (setting != 1 && setting != 2) return STREAMKL_ERR_INVALID_ARG;
     const int mode = opt ? opt->bwd_mode : 0;
     if (mode < 0 || mode > 2) return STREAMKL_ERR_INVALID_ARG;
-    if (opt && (opt->reserved != 0 || (opt->debug_flags & ~STREAMKL_DEBUG_INJECT_STALL))) return STREAMKL_ERR_INVALID_ARG;
+    if (opt && ((opt->grad_bf16 != 0 && opt->grad_bf16 != 1) || (opt->debug_flags & ~STREAMKL_DEBUG_INJECT_STALL)))
+        return STREAMKL_ERR_INVALID_ARG;
     if (mode == 1 && s->d != 128) return STREAMKL_ERR_UNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
@@ -135,7 +138,10 @@ streamkl_status plan_bwd(const streamkl_shape* s, int setting, int causal, const
     if (ctas_kv > INT32_MAX || ctas_q > INT32_MAX) return STREAMKL_ERR_UNSUPPORTED;
     pl->ctas_kv = static_cast<int>(ctas_kv);
     pl->ctas_q = static_cast<int>(ctas_q);
+    pl->bf16 = opt && opt->grad_bf16 == 1;
     pl->ws_bytes = kStatusBytes;
+    // bf16 gradients from the fused mode: dQ is accumulated in float32 in the workspace first
+    if (pl->fused && pl->bf16) pl->ws_bytes += size_t(BH) * s->Nq * s->d * sizeof(float);
     return STREAMKL_OK;
 }
 
@@ -287,14 +293,14 @@ streamkl_status streamkl_bwd_plan(const streamkl_shape* shape, int setting, int 
     plan->path = pl.fused ? 2 : 3;
     plan->num_splits = 1;
     plan->num_ctas = pl.ctas_kv;
-    plan->launches = 2;  // fused: zero dQ + kernel; split: two kernels
+    plan->launches = (pl.fused && pl.bf16) ? 3 : 2;  // fused: zero dQ + kernel (+ bf16 conversion); split: two kernels
     plan->workspace_bytes = pl.ws_bytes;
     return STREAMKL_OK;
 }
 
 streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const float* g, const void* Q1,
                              const void* K1, const void* Q2, const void* K2, const float* KL, const float* LSE1,
-                             const float* LSE2, float scale, int causal, float* dQ, float* dK, void* workspace,
+                             const float* LSE2, float scale, int causal, void* dQ, void* dK, void* workspace,
                              size_t workspace_bytes, const streamkl_options* opt, streamkl_stream_t stream) {
     streamkl_status st = check_shape(shape, causal);
     if (st != STREAMKL_OK) return st;
@@ -329,6 +335,10 @@ streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const flo
     p.LSE2 = LSE2;
     p.dQ = dQ;
     p.dK = dK;
+    p.grad_bf16 = pl.bf16 ? 1 : 0;
+    p.dQacc = pl.fused ? (pl.bf16 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes)
+                                  : static_cast<float*>(dQ))
+                       : nullptr;
     p.status = static_cast<unsigned int*>(workspace);
     p.wait_ns = static_cast<unsigned long long>(wait_limit(opt));
     p.inject_stall = (opt && (opt->debug_flags & STREAMKL_DEBUG_INJECT_STALL)) ? 1 : 0;
@@ -343,9 +353,14 @@ streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const flo
     pkv.num_q_tiles = (shape->Nq + 63) / 64;
     pkv.num_k_tiles = (shape->Nk + kBlockK - 1) / kBlockK;
     if (pl.fused) {
-        const size_t dq_bytes = size_t(shape->B) * shape->H * shape->Nq * shape->d * sizeof(float);
-        if (cudaMemsetAsync(dQ, 0, dq_bytes, s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+        const size_t dq_elems = size_t(shape->B) * shape->H * shape->Nq * shape->d;
+        if (cudaMemsetAsync(p.dQacc, 0, dq_elems * sizeof(float), s) != cudaSuccess) return STREAMKL_ERR_CUDA;
         if (launch_bwd_kv(shape->d, setting, true, kv, pkv, pl.ctas_kv, s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+        if (pl.bf16) {
+            int sms = 0;
+            if (device_sms(&sms) != STREAMKL_OK) return STREAMKL_ERR_CUDA;
+            if (launch_to_bf16(p.dQacc, dQ, dq_elems, sms, s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+        }
         return STREAMKL_OK;
     }
     // query-tile kernel: Q boxes of 128 rows, K boxes of 64 rows

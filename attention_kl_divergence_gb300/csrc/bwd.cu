@@ -16,6 +16,8 @@
 //                  visited once).
 // The split mode runs both kernels (each recomputes the scores); the fused
 // mode runs bwd_kv_kernel<FUSED> alone after zeroing dQ.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -89,6 +91,24 @@ __device__ __forceinline__ void store_ds_chunk(uint32_t tile_hi, uint32_t tile_l
         const uint32_t off = roff + (((chunk0 + cc) ^ (row & 7)) << 4);
         st_shared_v4(tile_hi + off, hi[0], hi[1], hi[2], hi[3]);
         st_shared_v4(tile_lo + off, lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+// Store 32 gradient values (scaled) at columns [c0, c0 + 32) of a row, as
+// float32 or as bf16 (round to nearest even).
+__device__ __forceinline__ void store_grad32(void* row, int c0, const float (&v)[32], float scale, bool bf16) {
+    if (bf16) {
+        uint4* out = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(row) + c0);
+#pragma unroll
+        for (int e = 0; e < 32; e += 8)
+            out[e / 8] = make_uint4(pack_bf16(v[e] * scale, v[e + 1] * scale), pack_bf16(v[e + 2] * scale, v[e + 3] * scale),
+                                    pack_bf16(v[e + 4] * scale, v[e + 5] * scale),
+                                    pack_bf16(v[e + 6] * scale, v[e + 7] * scale));
+    } else {
+        float4* out = reinterpret_cast<float4*>(reinterpret_cast<float*>(row) + c0);
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+            out[e / 4] = make_float4(v[e] * scale, v[e + 1] * scale, v[e + 2] * scale, v[e + 3] * scale);
     }
 }
 
@@ -325,18 +345,13 @@ __global__ void __launch_bounds__(320, 1)
         // epilogue: dQ row = scale * accumulator; each warpgroup writes half the columns
         if (ok && wait_all(base + L::bar_done, 0, wc, kErrWaitOther)) {
             tc_fence_after();
-            float* out = p.dQ + grow * D;
+            void* out = reinterpret_cast<uint8_t*>(p.dQ) + grow * D * (p.grad_bf16 ? 2 : 4);
 #pragma unroll 1
             for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 32) {
                 float v[32];
                 tmem_ld32(tl + 256 + c0, v);
                 tc_wait_ld();
-                if (i < p.Nq) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4*>(out + c0 + e) =
-                            make_float4(v[e] * p.scale, v[e + 1] * p.scale, v[e + 2] * p.scale, v[e + 3] * p.scale);
-                }
+                if (i < p.Nq) store_grad32(out, c0, v, p.scale, p.grad_bf16 != 0);
             }
         }
     }
@@ -648,18 +663,14 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
         // epilogue: dK row = scale * accumulator; each warpgroup writes half the columns
         if (ok && wait_all(base + L::bar_done, 0, wc, kErrWaitOther)) {
             tc_fence_after();
-            float* out = p.dK + (static_cast<size_t>(bkv) * p.Nk + j) * D;
+            void* out = reinterpret_cast<uint8_t*>(p.dK) +
+                        (static_cast<size_t>(bkv) * p.Nk + j) * D * (p.grad_bf16 ? 2 : 4);
 #pragma unroll 1
             for (int c0 = wg * (D / 2); c0 < (wg + 1) * (D / 2); c0 += 32) {
                 float v[32];
                 tmem_ld32(tl + 256 + c0, v);
                 tc_wait_ld();
-                if (key_ok) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        *reinterpret_cast<float4*>(out + c0 + e) =
-                            make_float4(v[e] * p.scale, v[e + 1] * p.scale, v[e + 2] * p.scale, v[e + 3] * p.scale);
-                }
+                if (key_ok) store_grad32(out, c0, v, p.scale, p.grad_bf16 != 0);
             }
         }
     } else if (FUSED) {
@@ -708,7 +719,7 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
             const int r0 = qtile(m) * kBwdTile;
             const int nrow = min(kBwdTile, p.Nq - r0);
             if (leader && nrow > 0) {
-                bulk_reduce_add_f32(p.dQ + ((static_cast<size_t>(b) * p.H + qhead(m)) * p.Nq + r0) * D, stage,
+                bulk_reduce_add_f32(p.dQacc + ((static_cast<size_t>(b) * p.H + qhead(m)) * p.Nq + r0) * D, stage,
                                     static_cast<uint32_t>(nrow * D * 4));
                 bulk_commit();
             }
@@ -722,6 +733,15 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+    }
+}
+
+// float32 -> bf16 (round to nearest even), 8 elements per thread and step.
+__global__ void __launch_bounds__(256) to_bf16_kernel(const float4* __restrict__ in, uint4* __restrict__ out,
+                                                      size_t n8) {
+    for (size_t k = blockIdx.x * size_t(blockDim.x) + threadIdx.x; k < n8; k += size_t(gridDim.x) * blockDim.x) {
+        const float4 a = in[2 * k], b = in[2 * k + 1];
+        out[k] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
     }
 }
 
@@ -759,6 +779,14 @@ cudaError_t launch_bwd_q(int d, int setting, const CUtensorMap* maps, const BwdP
     if (d == 128) return setting == 1 ? launch_q_impl<128, 1>(maps, p, ctas, stream)
                                       : launch_q_impl<128, 2>(maps, p, ctas, stream);
     return setting == 1 ? launch_q_impl<64, 1>(maps, p, ctas, stream) : launch_q_impl<64, 2>(maps, p, ctas, stream);
+}
+
+cudaError_t launch_to_bf16(const float* in, void* out, size_t n, int sms, cudaStream_t stream) {
+    const size_t n8 = n / 8;  // n is a multiple of 64 (rows of d = 64 or 128 elements)
+    const int blocks = static_cast<int>(std::min<size_t>((n8 + 255) / 256, size_t(sms) * 8));
+    to_bf16_kernel<<<blocks > 0 ? blocks : 1, 256, 0, stream>>>(reinterpret_cast<const float4*>(in),
+                                                               reinterpret_cast<uint4*>(out), n8);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_kv(int d, int setting, bool fused, const CUtensorMap* maps, const BwdParams& p, int ctas,

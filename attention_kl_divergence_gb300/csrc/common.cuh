@@ -57,8 +57,10 @@ struct BwdParams {
     const float* KL;
     const float* LSE1;
     const float* LSE2;
-    float* dQ;           // [B*H*Nq, d]
-    float* dK;           // [B*H_kv*Nk, d]
+    void* dQ;            // [B*H*Nq, d] float32 or bf16 (grad_bf16)
+    void* dK;            // [B*H_kv*Nk, d] float32 or bf16
+    float* dQacc;        // fused mode: float32 [B*H*Nq, d] the dQ tiles are added into
+    int grad_bf16;
     unsigned int* status;
     unsigned long long wait_ns;
     int inject_stall;

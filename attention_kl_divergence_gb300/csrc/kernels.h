@@ -18,6 +18,7 @@ int fwd_tile_stages(int d);
 // Q boxes of 64 rows, K boxes of 128 rows.
 cudaError_t launch_bwd_q(int d, int setting, const CUtensorMap* maps, const BwdParams& p, int ctas,
                          cudaStream_t stream);
+cudaError_t launch_to_bf16(const float* in, void* out, size_t n, int sms, cudaStream_t stream);
 cudaError_t launch_bwd_kv(int d, int setting, bool fused, const CUtensorMap* maps, const BwdParams& p, int ctas,
                           cudaStream_t stream);
 

@@ -35,7 +35,7 @@ class Shape(ctypes.Structure):
 
 class Options(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int32), ("bwd_mode", ctypes.c_int32), ("wait_limit_ns", ctypes.c_int64),
-                ("debug_flags", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("debug_flags", ctypes.c_int32), ("grad_bf16", ctypes.c_int32)]
 
 
 DEBUG_INJECT_STALL = 1
@@ -132,8 +132,8 @@ def _check_qk(Q1, K1, Q2, K2):
         raise ValueError("the key head count must divide the query head count")
 
 
-def _opts(num_splits=0, bwd_mode=0, wait_limit_ns=0, debug_flags=0):
-    return Options(int(num_splits), int(bwd_mode), int(wait_limit_ns), int(debug_flags), 0)
+def _opts(num_splits=0, bwd_mode=0, wait_limit_ns=0, debug_flags=0, grad_bf16=0):
+    return Options(int(num_splits), int(bwd_mode), int(wait_limit_ns), int(debug_flags), int(grad_bf16))
 
 
 def fwd_plan(Q1, K1, causal=False, num_splits=0) -> Plan:
@@ -143,11 +143,20 @@ def fwd_plan(Q1, K1, causal=False, num_splits=0) -> Plan:
     return plan
 
 
-def bwd_plan(Q1, K1, setting, causal=False, mode=BWD_AUTO) -> Plan:
+def bwd_plan(Q1, K1, setting, causal=False, mode=BWD_AUTO, grad_dtype=torch.float32) -> Plan:
     plan = Plan()
     _raise(load().streamkl_bwd_plan(ctypes.byref(make_shape(Q1, K1)), int(setting), int(bool(causal)),
-                                    ctypes.byref(_opts(bwd_mode=mode)), ctypes.byref(plan)), "streamkl_bwd_plan")
+                                    ctypes.byref(_opts(bwd_mode=mode, grad_bf16=_grad_flag(grad_dtype))),
+                                    ctypes.byref(plan)), "streamkl_bwd_plan")
     return plan
+
+
+def _grad_flag(grad_dtype):
+    if grad_dtype == torch.float32:
+        return 0
+    if grad_dtype == torch.bfloat16:
+        return 1
+    raise ValueError(f"gradients are float32 or bfloat16, not {grad_dtype}")
 
 
 def new_workspace(nbytes, device) -> torch.Tensor:
@@ -180,14 +189,14 @@ def kl_fwd(Q1, K1, Q2, K2, causal=False, scale=None, num_splits=0, workspace=Non
 
 
 def kl_bwd(setting, g, Q1, K1, Q2, K2, KL, LSE1, LSE2, causal=False, scale=None, mode=BWD_AUTO, workspace=None,
-           out=None, wait_limit_ns=0, debug_flags=0):
+           out=None, wait_limit_ns=0, debug_flags=0, grad_dtype=torch.float32):
     """(dQ, dK) float32 of the trainable side: setting 1 -> (Q2, K2), 2 -> (Q1, K1).
     With keys shared by groups of query heads (K has fewer heads than Q), dK
     has K's head count and sums the gradients of each group."""
     _check_qk(Q1, K1, Q2, K2)
     lib = load()
     shape = make_shape(Q1, K1)
-    opts = _opts(0, mode, wait_limit_ns, debug_flags)
+    opts = _opts(0, mode, wait_limit_ns, debug_flags, _grad_flag(grad_dtype))
     plan = Plan()
     _raise(lib.streamkl_bwd_plan(ctypes.byref(shape), int(setting), int(bool(causal)), ctypes.byref(opts),
                                  ctypes.byref(plan)), "streamkl_bwd_plan")
@@ -197,8 +206,11 @@ def kl_bwd(setting, g, Q1, K1, Q2, K2, KL, LSE1, LSE2, causal=False, scale=None,
         if t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != (B, H, Nq):
             raise ValueError(f"{name} must be contiguous float32 [B, H, Nq]")
     if out is None:
-        out = (torch.empty((B, H, Nq, d), dtype=torch.float32, device=Q1.device),
-               torch.empty((B, K1.shape[1], Nk, d), dtype=torch.float32, device=Q1.device))
+        out = (torch.empty((B, H, Nq, d), dtype=grad_dtype, device=Q1.device),
+               torch.empty((B, K1.shape[1], Nk, d), dtype=grad_dtype, device=Q1.device))
+    for t in out:
+        if t.dtype != grad_dtype or not t.is_contiguous():
+            raise ValueError("gradient outputs must be contiguous tensors of grad_dtype")
     if workspace is None or workspace.numel() < plan.workspace_bytes:
         workspace = new_workspace(plan.workspace_bytes, Q1.device)
     dQ, dK = out
@@ -244,8 +256,7 @@ class AttentionKL(torch.autograd.Function):
             return (None,) * 6
         setting = 1 if student else 2
         dQ, dK = kl_bwd(setting, gKL.float().contiguous(), Q1, K1, Q2, K2, KL, L1, L2, causal=ctx.causal,
-                        scale=ctx.scale)
-        dQ, dK = dQ.to(Q1.dtype), dK.to(K1.dtype)
+                        scale=ctx.scale, grad_dtype=torch.bfloat16)
         if setting == 1:
             return None, None, dQ, dK, None, None
         return dQ, dK, None, None, None, None

@@ -24,9 +24,10 @@
  *    streamkl_shape and must be multiples of 8 elements (16 bytes).  Q1 and
  *    Q2 share one set of strides, K1 and K2 another.  Base pointers must be
  *    16-byte aligned.  d must be 64 or 128.
- *  - KL, LSE1, LSE2 and g are float32 [B, H, Nq], contiguous.  dQ is float32
- *    [B, H, Nq, d] and dK float32 [B, H_kv, Nk, d], contiguous; with shared
- *    keys dK sums the gradients of every query head of the group.
+ *  - KL, LSE1, LSE2 and g are float32 [B, H, Nq], contiguous.  dQ is
+ *    [B, H, Nq, d] and dK [B, H_kv, Nk, d], contiguous, float32 (or bf16 on
+ *    request); with shared keys dK sums the gradients of every query head of
+ *    the group.
  *  - Logarithms are natural.  LSE_t[i] = log sum_j exp(S_t[i,j]) includes the
  *    softmax scale.
  *  - causal != 0 aligns the mask bottom-right: row i sees keys
@@ -86,7 +87,7 @@ typedef struct {
                            /*           2 = separate dQ and dK kernels                */
     int64_t wait_limit_ns; /* limit of every in-kernel wait; 0 = default (2 s)      */
     int32_t debug_flags;   /* 0 in normal use; see STREAMKL_DEBUG_*                  */
-    int32_t reserved;      /* must be 0                                              */
+    int32_t grad_bf16;     /* backward: 0 = float32 dQ/dK, 1 = bf16 dQ/dK            */
 } streamkl_options;
 
 /* Test aid for the bounded waits: the first CTA of the main kernel waits on a
@@ -130,11 +131,13 @@ STREAMKL_API streamkl_status streamkl_bwd_plan(const streamkl_shape* shape, int 
  *   setting 2 (student fixed): dQ = dL/dQ1, dK = dL/dK1,
  *                              dS1 = g P1 ((S1 - LSE1) - (S2 - LSE2) - KL)
  * and dQ = scale * dS K, dK = scale * dS^T Q.  KL, LSE1, LSE2 are the
- * forward's outputs for the same inputs.  dQ and dK are overwritten.
+ * forward's outputs for the same inputs.  dQ and dK are overwritten; they are
+ * float32 unless opt->grad_bf16 selects bf16 (the fused mode then also needs
+ * 4 bytes per dQ element of workspace to accumulate in float32).
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
 STREAMKL_API streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const float* g, const void* Q1,
                              const void* K1, const void* Q2, const void* K2, const float* KL, const float* LSE1,
-                             const float* LSE2, float scale, int causal, float* dQ, float* dK, void* workspace,
+                             const float* LSE2, float scale, int causal, void* dQ, void* dK, void* workspace,
                              size_t workspace_bytes, const streamkl_options* opt, streamkl_stream_t stream);
 
 /* Size of the library's own built-in scratch buffer used by streamkl_fwd_noalloc. */

@@ -75,7 +75,7 @@ def test_workspace_status_rejects_null():
 def test_options_reject_unknown_debug_flags_without_device():
     lib = sk.load()
     P = ctypes.c_void_p
-    bad = sk.Options(0, 0, 0, 8, 0)
+    bad = sk.Options(0, 0, 0, 8, 0)  # unknown debug flag
     rc = lib.streamkl_fwd(ctypes.byref(_shape()), *[P(256)] * 4, ctypes.c_float(0.0), 0, *[P(256)] * 3, P(256),
                           4096, ctypes.byref(bad), P(0))
     assert rc in (sk.ERR_INVALID_ARG, sk.ERR_CUDA)  # the option check needs no device but runs in the planner

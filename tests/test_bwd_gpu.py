@@ -153,3 +153,29 @@ def test_bnhd_layout_views_backward(setting, mode):
     rdQ, rdK = oracle.bwd(setting, g, *base, causal=True)
     assert_grad(dQ, rdQ, "dQ (B N H d views)")
     assert_grad(dK, rdK, "dK (B N H d views)")
+
+
+@pytest.mark.parametrize("setting", [1, 2])
+@pytest.mark.parametrize("mode", [FUSED, SPLIT])
+def test_bf16_gradient_outputs(setting, mode):
+    """grad_dtype=bf16: the same gradients, rounded once to bf16 on output."""
+    Q1, K1, Q2, K2 = make_qk(1, 2, 300, 300, 128, 0.4, seed=23, device=DEV)
+    g = torch.rand((1, 2, 300), device=DEV) + 0.5
+    KL, L1, L2 = streamkl.kl_fwd(Q1, K1, Q2, K2, causal=True)
+    plan = streamkl.bwd_plan(Q1, K1, setting, True, mode, grad_dtype=torch.bfloat16)
+    dQ, dK = streamkl.kl_bwd(setting, g, Q1, K1, Q2, K2, KL, L1, L2, causal=True, mode=mode,
+                             grad_dtype=torch.bfloat16)
+    f32 = streamkl.kl_bwd(setting, g, Q1, K1, Q2, K2, KL, L1, L2, causal=True, mode=mode)
+    torch.cuda.synchronize()
+    assert dQ.dtype == torch.bfloat16 and dK.dtype == torch.bfloat16
+    assert plan.launches == (3 if mode == FUSED else 2)
+    rdQ, rdK = oracle.bwd(setting, g, Q1, K1, Q2, K2, causal=True)
+    assert_grad(dQ.float(), rdQ, "dQ (bf16 output)")
+    assert_grad(dK.float(), rdK, "dK (bf16 output)")
+    # bf16 output = float32 output rounded to nearest even.  The fused mode adds dQ tiles in
+    # no fixed order, so two runs may differ in the last float32 bits: allow one bf16 ulp there.
+    torch.testing.assert_close(dK, f32[1].to(torch.bfloat16), rtol=0, atol=0)
+    if mode == FUSED:
+        torch.testing.assert_close(dQ.float(), f32[0].to(torch.bfloat16).float(), rtol=2.0 ** -7, atol=1e-30)
+    else:
+        torch.testing.assert_close(dQ, f32[0].to(torch.bfloat16), rtol=0, atol=0)
