@@ -114,8 +114,8 @@ struct BwdPlan {
 // float32 dQ buffer fits in L2 and separate kernels beyond.  Measured on
 // GB300 the fused kernel is faster at every size tried (8K causal 2.0 vs
 // 2.5 ms, 64K causal 108 vs 138 ms: the split pays a second recompute of both
-// score tiles, which costs more than the L2 atomics), so the automatic choice
-// is fused whenever its dQ^T tile is available (d = 128) and split otherwise.
+// score tiles, which costs more than the L2 reductions), so the automatic
+// choice is always fused; the split stays selectable.
 streamkl_status plan_bwd(const streamkl_shape* s, int setting, int causal, const streamkl_options* opt,
                          BwdPlan* pl) {
     streamkl_status st = check_shape(s, causal);
@@ -125,12 +125,11 @@ streamkl_status plan_bwd(const streamkl_shape* s, int setting, int causal, const
     if (mode < 0 || mode > 2) return STREAMKL_ERR_INVALID_ARG;
     if (opt && ((opt->grad_bf16 != 0 && opt->grad_bf16 != 1) || (opt->debug_flags & ~STREAMKL_DEBUG_INJECT_STALL)))
         return STREAMKL_ERR_INVALID_ARG;
-    if (mode == 1 && s->d != 128) return STREAMKL_ERR_UNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
     const int64_t BH = int64_t(s->B) * s->H;
     if (mode == 0)
-        pl->fused = s->d == 128;
+        pl->fused = true;
     else
         pl->fused = mode == 1;
     const int64_t ctas_kv = int64_t(s->B) * kv_heads(s) * ((s->Nk + kBlockK - 1) / kBlockK);

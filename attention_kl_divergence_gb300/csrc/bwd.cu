@@ -386,7 +386,10 @@ struct KvSmem {
     static constexpr int q = 2 * kKBytes;
     static constexpr int kNumDs = 2;                   // dS buffers (hi + lo each)
     static constexpr int ds = q + 2 * NST * kQBytes;   // buffer b: hi at ds + 2*b*kDsBytes, lo right after
-    static constexpr int vec = ds + 2 * kNumDs * kDsBytes;  // [NST][3][64] floats
+    // d = 64: a zero 64-feature atom pads the dQ^T MMA's A operand (K_t^T) to M = 128
+    static constexpr int zero = ds + 2 * kNumDs * kDsBytes;
+    static constexpr int kZeroBytes = D < 128 ? kBlockK * 128 : 0;
+    static constexpr int vec = zero + kZeroBytes;  // [NST][3][64] floats
     static constexpr int bars = vec + NST * 3 * kBwdTile * 4;
     static constexpr int bar_k = bars;
     static constexpr int bar_qfull = bar_k + 8;
@@ -437,8 +440,8 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
     const int per_head = p.num_q_tiles - m_start;  // query tiles of one query head that see this key tile
     const int n_tiles = per_head * p.kv_group;
     // iteration m -> (query head, query tile)
-    auto qhead = [&](int m) { return hk * p.kv_group + m / per_head; };
-    auto qtile = [&](int m) { return m_start + m % per_head; };
+    auto qhead = [&](int m) { return p.kv_group == 1 ? hk : hk * p.kv_group + m / per_head; };
+    auto qtile = [&](int m) { return m_start + (p.kv_group == 1 ? m : m % per_head); };
     const uint32_t kt_tile = base + (SETTING == 1 ? L::k2 : L::k1);  // trainable keys
     const uint32_t qt_off = SETTING == 1 ? L::kQBytes : 0;           // trainable queries within a stage
 
@@ -460,6 +463,11 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
+    }
+    if (L::kZeroBytes > 0) {
+        for (int k = threadIdx.x; k < L::kZeroBytes / 16; k += blockDim.x)
+            st_shared_v4(base + L::zero + 16 * k, 0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();  // the tensor core reads it through the async proxy
     }
     if (warp == 1) tmem_alloc(base + L::misc, 512);
     tc_fence_before();
@@ -524,7 +532,9 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_bf16_f32(kBlockK, kBwdTile);
             constexpr uint32_t id_dk = idesc_bf16_f32(kBlockK, D, 0, 1);
-            constexpr uint32_t id_dq = idesc_bf16_f32(D, 2 * kBwdTile, 1, 1);
+            constexpr uint32_t id_dq = idesc_bf16_f32(128, 2 * kBwdTile, 1, 1);  // M = 128 features (d = 64: padded)
+            // A = K_t^T as 64-feature atoms: the tile's second block, or the zero atom when d = 64
+            const uint32_t a_atom = D == 128 ? kBlockK * 128 : base + L::zero - kt_tile;
             const uint32_t t_k = tmem, t_s = tmem + 128, t_dk = tmem + 256, t_dq = tmem + 384;
             int issued = 0;
             bool started = false;
@@ -585,7 +595,7 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
                             tc_fence_after();
 #pragma unroll
                             for (int kk = 0; kk < kBlockK / 16; ++kk)
-                                tc_mma_bf16(t_dq, smem_desc_mn128(kt_tile + kk * 16 * 128, kBlockK * 128),
+                                tc_mma_bf16(t_dq, smem_desc_mn128(kt_tile + kk * 16 * 128, a_atom),
                                             smem_desc_mn128(dss + kk * 16 * 128, L::kDsBytes), id_dq, kk > 0);
                             tc_commit(base + L::bar_dqfull);
                         }
@@ -689,7 +699,7 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
             if (!bar_sync_and(3, 128, wait_all(base + L::bar_dqfull, m & 1, wc, kErrWaitOther))) break;
             tc_fence_after();
             float v0[32], v1[32];
-            {
+            if (wq * 32 < D) {  // d = 64: TMEM lanes 64-127 hold the zero padding
                 float lo[32];
                 tmem_ld32(tl + 384, v0);  // hi half, query rows 0-31
                 tmem_ld32(tl + 448, lo);  // lo half, query rows 0-31
@@ -706,13 +716,15 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
             mbar_arrive(base + L::bar_dqempty);
             if (leader) bulk_wait_read_all();  // the previous tile's reduction has read the stage
             asm volatile("bar.sync 2, 128;" ::: "memory");
+            if (f < D) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                asm volatile("st.shared.f32 [%0], %1;" ::"r"(stage + e * (D * 4) + f * 4), "f"(v0[e] * p.scale)
-                             : "memory");
-                asm volatile("st.shared.f32 [%0], %1;" ::"r"(stage + (e + 32) * (D * 4) + f * 4),
-                             "f"(v1[e] * p.scale)
-                             : "memory");
+                for (int e = 0; e < 32; ++e) {
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(stage + e * (D * 4) + f * 4), "f"(v0[e] * p.scale)
+                                 : "memory");
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(stage + (e + 32) * (D * 4) + f * 4),
+                                 "f"(v1[e] * p.scale)
+                                 : "memory");
+                }
             }
             fence_proxy_async_smem();
             asm volatile("bar.sync 2, 128;" ::: "memory");
@@ -798,7 +810,9 @@ cudaError_t launch_bwd_kv(int d, int setting, bool fused, const CUtensorMap* map
         return setting == 1 ? launch_kv_impl<128, 1, false>(maps, p, ctas, stream)
                             : launch_kv_impl<128, 2, false>(maps, p, ctas, stream);
     }
-    if (fused) return cudaErrorInvalidValue;  // the fused dQ^T MMA needs M = d = 128
+    if (fused)
+        return setting == 1 ? launch_kv_impl<64, 1, true>(maps, p, ctas, stream)
+                            : launch_kv_impl<64, 2, true>(maps, p, ctas, stream);
     return setting == 1 ? launch_kv_impl<64, 1, false>(maps, p, ctas, stream)
                         : launch_kv_impl<64, 2, false>(maps, p, ctas, stream);
 }

@@ -68,6 +68,9 @@ WORKLOADS = {
     # one batch of the 128K decode: small enough for a full ncu capture (2 GiB of keys)
     "decode_q1_k128k_b1": Workload("decode_q1_k128k_b1", 1, 32, 1, 131072, 128, 0.3, False, seed=3,
                                    fwd_only=True),
+    # head dimension 64 (the tiny case's d) at 8K and 64K context
+    "8k_causal_d64": Workload("8k_causal_d64", 1, 32, 8192, 8192, 64, 0.3, True, seed=6),
+    "64k_causal_d64": Workload("64k_causal_d64", 1, 32, 65536, 65536, 64, 0.3, True, seed=6),
     "512k_causal": Workload("512k_causal", 1, 8, 524288, 524288, 128, 0.3, True, teacher_scale=1.5, seed=4),
 }
 

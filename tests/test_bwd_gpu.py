@@ -52,13 +52,16 @@ def test_shapes_d128(B, H, Nq, Nk, causal, setting, mode):
     check_full(setting, Q1, K1, Q2, K2, g, causal, mode)
 
 
+@pytest.mark.parametrize("mode", [FUSED, SPLIT])
 @pytest.mark.parametrize("setting", [1, 2])
-@pytest.mark.parametrize("B,H,Nq,Nk,causal", [(1, 2, 190, 190, True), (2, 1, 100, 300, False)])
-def test_shapes_d64_split(B, H, Nq, Nk, causal, setting):
+@pytest.mark.parametrize("B,H,Nq,Nk,causal", [(1, 2, 190, 190, True), (2, 1, 100, 300, False), (1, 1, 1, 500, False)])
+def test_shapes_d64(B, H, Nq, Nk, causal, setting, mode):
+    """d = 64: the fused kernel pads its dQ^T MMA to 128 features with a zero atom."""
     Q1, K1, Q2, K2 = make_qk(B, H, Nq, Nk, 64, 0.5, seed=Nq + 11 * Nk, device=DEV)
     g = torch.rand((B, H, Nq), device=DEV) + 0.5
-    assert streamkl.bwd_plan(Q1, K1, setting, causal).path == streamkl.PATH_BWD_SPLIT
-    check_full(setting, Q1, K1, Q2, K2, g, causal, streamkl.BWD_AUTO)
+    expect = streamkl.PATH_BWD_FUSED if mode == FUSED else streamkl.PATH_BWD_SPLIT
+    assert streamkl.bwd_plan(Q1, K1, setting, causal, mode).path == expect
+    check_full(setting, Q1, K1, Q2, K2, g, causal, mode)
 
 
 def test_fused_and_split_agree():
