@@ -32,6 +32,7 @@ class Workload:
     teacher_scale: float = 1.0
     seed: int = 0
     fwd_only: bool = False  # the decode (Split-K) workloads run the forward only
+    H_kv: int = 0           # key heads when keys are shared by groups of query heads (0 = H)
 
     @property
     def g_value(self) -> float:
@@ -41,7 +42,8 @@ class Workload:
     def fwd_bytes(self) -> int:
         """Algorithmic HBM bytes of one forward: every Q and K element read once
         (bf16) and KL, LSE1, LSE2 written once (float32)."""
-        return 2 * 2 * self.B * self.H * (self.Nq + self.Nk) * self.d + 12 * self.B * self.H * self.Nq
+        hk = self.H_kv or self.H
+        return 2 * 2 * self.B * (self.H * self.Nq + hk * self.Nk) * self.d + 12 * self.B * self.H * self.Nq
 
     def visible_pairs(self) -> int:
         """Query/key pairs inside the mask, per head.  Causal rows are aligned
@@ -65,6 +67,9 @@ WORKLOADS = {
     # causal (bottom-right) Split-K: 16 new queries against a 128K-key prefix (chunked prefill)
     "decode_causal_q16_k128k": Workload("decode_causal_q16_k128k", 4, 32, 16, 131072, 128, 0.3, True, seed=5,
                                         fwd_only=True),
+    # decode with keys shared by groups of 4 query heads (32 query heads, 8 key heads)
+    "decode_gqa_q1_k128k": Workload("decode_gqa_q1_k128k", 4, 32, 1, 131072, 128, 0.3, False, seed=7,
+                                    fwd_only=True, H_kv=8),
     # one batch of the 128K decode: small enough for a full ncu capture (2 GiB of keys)
     "decode_q1_k128k_b1": Workload("decode_q1_k128k_b1", 1, 32, 1, 131072, 128, 0.3, False, seed=3,
                                    fwd_only=True),
@@ -75,26 +80,28 @@ WORKLOADS = {
 }
 
 
-def make_qk(B, H, Nq, Nk, d, sigma, teacher_scale=1.0, seed=0, device="cpu"):
-    """(Q1, K1, Q2, K2) as contiguous bf16 [B, H, N, d] tensors on ``device``."""
+def make_qk(B, H, Nq, Nk, d, sigma, teacher_scale=1.0, seed=0, device="cpu", H_kv=0):
+    """(Q1, K1, Q2, K2) as contiguous bf16 [B, H, N, d] tensors on ``device``
+    (K1, K2 with H_kv heads when H_kv is given)."""
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
+    hk = H_kv or H
 
-    def draw(n):
-        return torch.randn((B, H, n, d), generator=gen, device=device, dtype=torch.float32)
+    def draw(heads, n):
+        return torch.randn((B, heads, n, d), generator=gen, device=device, dtype=torch.float32)
 
-    Q1 = draw(Nq)
-    K1 = draw(Nk)
+    Q1 = draw(H, Nq)
+    K1 = draw(hk, Nk)
     if teacher_scale != 1.0:
         Q1.mul_(teacher_scale)
         K1.mul_(teacher_scale)
-    Q2 = draw(Nq).mul_(sigma).add_(Q1)
-    K2 = draw(Nk).mul_(sigma).add_(K1)
+    Q2 = draw(H, Nq).mul_(sigma).add_(Q1)
+    K2 = draw(hk, Nk).mul_(sigma).add_(K1)
     return tuple(t.to(torch.bfloat16).contiguous() for t in (Q1, K1, Q2, K2))
 
 
 def make_workload(w: Workload, device="cpu"):
-    return make_qk(w.B, w.H, w.Nq, w.Nk, w.d, w.sigma, w.teacher_scale, w.seed, device)
+    return make_qk(w.B, w.H, w.Nq, w.Nk, w.d, w.sigma, w.teacher_scale, w.seed, device, H_kv=w.H_kv)
 
 
 def make_g(B, H, Nq, value, device="cpu"):

@@ -101,7 +101,7 @@ def test_64k_noncausal_forward_and_both_settings():
 
 
 @pytest.mark.parametrize("name", ["decode_q1_k128k", "decode_q16_k128k", "decode_q1_k512k", "decode_q16_k512k",
-                                  "decode_causal_q16_k128k"])
+                                  "decode_causal_q16_k128k", "decode_gqa_q1_k128k"])
 def test_decode_split_k_all_rows_of_sampled_heads(name):
     w = WORKLOADS[name]
     inputs = make_workload(w, device=DEV)
@@ -109,8 +109,12 @@ def test_decode_split_k_all_rows_of_sampled_heads(name):
     assert plan.path == streamkl.PATH_DECODE and plan.num_splits > 1
     KL, L1, L2 = streamkl.kl_fwd(*inputs, causal=w.causal)
     torch.cuda.synchronize()
+    group = w.H // (w.H_kv or w.H)
     for bh in (0, 37, 64, w.B * w.H - 1):
-        rKL, rL1, rL2 = oracle.fwd(*[head(t, bh) for t in inputs], causal=w.causal)
+        b, h = divmod(bh, w.H)
+        q1, k1, q2, k2 = inputs
+        hq = [head(q1, bh), k1[b, h // group][None, None], head(q2, bh), k2[b, h // group][None, None]]
+        rKL, rL1, rL2 = oracle.fwd(*hq, causal=w.causal)
         assert_lse(L1.reshape(-1, w.Nq)[bh], rL1, f"LSE1 head {bh}")
         assert_lse(L2.reshape(-1, w.Nq)[bh], rL2, f"LSE2 head {bh}")
         assert_kl(KL.reshape(-1, w.Nq)[bh], rKL, f"KL head {bh}")
@@ -119,3 +123,7 @@ def test_decode_split_k_all_rows_of_sampled_heads(name):
 
 def test_512k_causal_forward_and_setting2():
     run_workload("512k_causal", (2,), heads=(0, 7), rows_per_head=24, key_tail=256, keys_per_head=12)
+
+
+def test_64k_causal_d64_forward_and_setting1():
+    run_workload("64k_causal_d64", (1,), heads=(0, 31), rows_per_head=32, key_tail=512, keys_per_head=16)
