@@ -67,6 +67,7 @@ int choose_splits(int64_t units, int k_tiles, int slots) {
 
 struct FwdPlan {
     bool decode;
+    int heads_per_cta;  // decode: query heads sharing a key head packed into one CTA
     int num_splits;
     int ctas;
     int num_q_tiles;
@@ -86,7 +87,17 @@ streamkl_status plan_fwd(const streamkl_shape* s, int causal, const streamkl_opt
     pl->decode = s->Nq <= kDecodeMaxQ;
     pl->num_q_tiles = pl->decode ? 1 : (s->Nq + kBlockQ - 1) / kBlockQ;
     pl->num_k_tiles = (s->Nk + kBlockK - 1) / kBlockK;
-    const int64_t units = BH * pl->num_q_tiles;
+    // decode: the largest divisor of the group whose queries fit the 16 columns
+    pl->heads_per_cta = 1;
+    if (pl->decode) {
+        const int group = s->H / kv_heads(s);
+        for (int c = group; c > 1; --c)
+            if (group % c == 0 && c * s->Nq <= kDecodeMaxQ) {
+                pl->heads_per_cta = c;
+                break;
+            }
+    }
+    const int64_t units = BH / pl->heads_per_cta * pl->num_q_tiles;
     int splits;
     if (opt && opt->num_splits > 0)
         splits = opt->num_splits < pl->num_k_tiles ? opt->num_splits : pl->num_k_tiles;
@@ -158,9 +169,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 4-D map over [B, H, N, d] bf16 with a (64 x rows) box, 128-byte swizzle;
-// rows outside [0, N) read as zero.
-bool make_map(CUtensorMap* m, const void* ptr, const streamkl_shape* s, bool is_q, int box_rows) {
+// 4-D map over [B, H, N, d] bf16 with a (64 x rows x heads) box, 128-byte
+// swizzle; rows outside [0, N) read as zero.  A box of several heads lands
+// in shared memory as heads * rows consecutive 128-byte rows, head-major.
+bool make_map(CUtensorMap* m, const void* ptr, const streamkl_shape* s, bool is_q, int box_rows,
+              int box_heads = 1) {
     auto enc = encode_fn();
     if (!enc) return false;
     const int64_t N = is_q ? s->Nq : s->Nk;
@@ -169,7 +182,7 @@ bool make_map(CUtensorMap* m, const void* ptr, const streamkl_shape* s, bool is_
     const int64_t sn = is_q ? s->q_stride_n : s->k_stride_n;
     cuuint64_t dims[4] = {cuuint64_t(s->d), cuuint64_t(N), cuuint64_t(is_q ? s->H : kv_heads(s)), cuuint64_t(s->B)};
     cuuint64_t strides[3] = {cuuint64_t(sn * 2), cuuint64_t(sh * 2), cuuint64_t(sb * 2)};
-    cuuint32_t box[4] = {cuuint32_t(kSwizzleCols), cuuint32_t(box_rows), 1, 1};
+    cuuint32_t box[4] = {cuuint32_t(kSwizzleCols), cuuint32_t(box_rows), cuuint32_t(box_heads), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -236,10 +249,12 @@ streamkl_status streamkl_fwd(const streamkl_shape* shape, const void* Q1, const 
     if ((st = plan_fwd(shape, causal, opt, &pl)) != STREAMKL_OK) return st;
     if (workspace_bytes < pl.ws_bytes) return STREAMKL_ERR_WORKSPACE;
 
-    const int qrows = pl.decode ? kDecodeMaxQ : kBlockQ;
+    // decode: one query box is the Nq rows of heads_per_cta heads
+    const int qrows = pl.decode ? shape->Nq : kBlockQ;
+    const int qheads = pl.heads_per_cta;
     CUtensorMap maps[4];
-    if (!make_map(&maps[0], Q1, shape, true, qrows) || !make_map(&maps[1], K1, shape, false, kBlockK) ||
-        !make_map(&maps[2], Q2, shape, true, qrows) || !make_map(&maps[3], K2, shape, false, kBlockK))
+    if (!make_map(&maps[0], Q1, shape, true, qrows, qheads) || !make_map(&maps[1], K1, shape, false, kBlockK) ||
+        !make_map(&maps[2], Q2, shape, true, qrows, qheads) || !make_map(&maps[3], K2, shape, false, kBlockK))
         return STREAMKL_ERR_CUDA;
 
     const float sc = resolve_scale(scale, shape->d);
@@ -254,6 +269,7 @@ streamkl_status streamkl_fwd(const streamkl_shape* shape, const void* Q1, const 
     p.causal = causal ? 1 : 0;
     p.diag_off = shape->Nk - shape->Nq;
     p.kv_group = shape->H / kv_heads(shape);
+    p.heads_per_cta = pl.heads_per_cta;
     p.scale = sc;
     p.scale_log2e = sc * 1.4426950408889634f;
     p.KL = KL;

@@ -31,6 +31,7 @@ struct FwdParams {
     int causal;          // bottom-right causal mask
     int diag_off;        // Nk - Nq
     int kv_group;        // query heads per key head (1 = no sharing)
+    int heads_per_cta;   // decode: query heads of one key head packed into a CTA's query columns
     float scale;         // softmax scale
     float scale_log2e;   // scale * log2(e): raw dot product -> base-2 exponent
     float* KL;           // [B*H*Nq]

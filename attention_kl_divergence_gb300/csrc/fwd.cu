@@ -13,6 +13,8 @@
 // Attention Distillation" (gist.science/paper/2606.20005, technical summary),
 // Methodology 1 (online formulation: m1, m2, l1, l2, acc with acc rescaled by
 // the teacher maximum; KL = acc/l1 + LSE2 - LSE1) and Methodology 3 (Split-K).
+#include <climits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -375,6 +377,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 // Decode forward, Nq <= 16 (causal or not).  S^T = K Q^T: M = 128 keys (TMEM lanes),
 // N = 16 query columns.  Each thread owns one key per step and keeps a running
 // state per query; the 128 states are merged at the end of the key range.
+// Query heads that share a key head are packed into the 16 columns
+// (heads_per_cta heads x Nq rows, head-major), so a shared key tile is
+// streamed once for all of them.
 // ---------------------------------------------------------------------------
 template <int D, int NST>
 struct DecodeSmem {
@@ -411,10 +416,14 @@ __global__ void __launch_bounds__(192, 1)
     float* red = reinterpret_cast<float*>(gbase + L::red);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x / p.num_splits;
-    const int split = blockIdx.x - bh * p.num_splits;
-    const int b = bh / p.H, h = bh - b * p.H;
-    const int hk = h / p.kv_group;  // key head (shared by kv_group query heads)
+    const int hp = p.heads_per_cta;
+    const int nq = hp * p.Nq;  // packed query columns in use
+    const int gi = blockIdx.x / p.num_splits;
+    const int split = blockIdx.x - gi * p.num_splits;
+    const int groups = p.H / hp;
+    const int b = gi / groups, h0 = (gi - b * groups) * hp;
+    const int hk = h0 / p.kv_group;  // key head shared by the packed query heads
+    const size_t row0 = (static_cast<size_t>(b) * p.H + h0) * p.Nq;  // output row of column 0
     const int per_split = (p.num_k_tiles + p.num_splits - 1) / p.num_splits;
     const int kt_begin = split * per_split;
     const int n_tiles = max(0, min(p.num_k_tiles, kt_begin + per_split) - kt_begin);
@@ -432,8 +441,15 @@ __global__ void __launch_bounds__(192, 1)
         mbar_init(base + L::bar_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
-        fence_proxy_async_smem();
     }
+    // unused query columns read zeros (the copies below fill only the first nq rows)
+    for (int i = threadIdx.x; i < 2 * (D / kSwizzleCols) * (NQ - nq) * 8; i += blockDim.x) {
+        const int chunk16 = i & 7, rr = i >> 3;
+        const int r = nq + rr % (NQ - nq), tc = rr / (NQ - nq);  // tc: tensor * column blocks
+        const uint32_t at = base + (tc & 1 ? L::q2 : L::q1) + (tc >> 1) * NQ * 128 + r * 128 + chunk16 * 16;
+        st_shared_v4(at, 0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
     if (warp == 1) tmem_alloc(base + L::misc, 64);
     tc_fence_before();
     __syncthreads();
@@ -448,11 +464,12 @@ __global__ void __launch_bounds__(192, 1)
             prefetch_tensormap(&tQ2);
             prefetch_tensormap(&tK2);
             const uint64_t stream_once = policy_evict_first();  // each key is read exactly once
-            mbar_arrive_expect_tx(base + L::bar_q, 2 * L::kQBytes);
+            // one box = Nq rows x heads_per_cta heads, landing as nq consecutive rows
+            mbar_arrive_expect_tx(base + L::bar_q, 2 * nq * D * 2);
 #pragma unroll
             for (int c = 0; c < D / kSwizzleCols; ++c) {
-                tma_load_4d(base + L::q1 + c * NQ * 128, &tQ1, base + L::bar_q, c * kSwizzleCols, 0, h, b);
-                tma_load_4d(base + L::q2 + c * NQ * 128, &tQ2, base + L::bar_q, c * kSwizzleCols, 0, h, b);
+                tma_load_4d(base + L::q1 + c * NQ * 128, &tQ1, base + L::bar_q, c * kSwizzleCols, 0, h0, b);
+                tma_load_4d(base + L::q2 + c * NQ * 128, &tQ2, base + L::bar_q, c * kSwizzleCols, 0, h0, b);
             }
             int it = 0;
             for (; it < n_tiles; ++it) {
@@ -519,10 +536,13 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const float c = p.scale_log2e;
         const float tau = kTau / c;
-        const int nq = p.Nq;
+        // query index within its head of each packed column; unused columns
+        // get INT_MIN, below every causal bound
+        int qi[NQ];
         float m1[NQ], l1[NQ], ac[NQ], m2[NQ], l2[NQ];
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
+            qi[q] = q < nq ? q % p.Nq : INT_MIN;
             m1[q] = -INFINITY;
             m2[q] = -INFINITY;
             l1[q] = l2[q] = ac[q] = 0.f;
@@ -543,12 +563,12 @@ __global__ void __launch_bounds__(192, 1)
             mbar_arrive(base + L::bar_sempty + 8 * buf);
             const int j = (kt_begin + it) * kBlockK + krow;
             if (j >= p.Nk) continue;  // key tail
-            // causal (bottom-right): query q sees key j iff j <= q + diag_off; keys up to
+            // causal (bottom-right): query i sees key j iff j <= i + diag_off; keys up to
             // diag_off are seen by every query
             const int first_q = p.causal ? j - p.diag_off : 0;
 #pragma unroll
             for (int q = 0; q < NQ; ++q) {
-                if (q < nq && q >= first_q) {
+                if (qi[q] >= first_q) {
                     if (z1[q] > m1[q] + tau) {
                         const float a = ex2(c * (m1[q] - z1[q]));
                         l1[q] *= a;
@@ -597,7 +617,7 @@ __global__ void __launch_bounds__(192, 1)
                 RowState t{r[0], r[1], r[2], r[3], r[4]};
                 merge_state(s, t, c);
             }
-            store_row(p, static_cast<size_t>(bh) * p.Nq + q, split, s, !ok || *abort_flag);
+            store_row(p, row0 + q, split, s, !ok || *abort_flag);
         }
     }
 
