@@ -552,55 +552,80 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
                     tc_cp_128x256b(t_k + D / 2 + kk * 8, smem_desc_k128(base + L::k2 + ko));
                 }
                 started = true;
+                // The update warps share this thread's scheduler and keep it busy while
+                // they form dS, so the issue loop runs as few instructions as it can:
+                // descriptor low words advance by compile-time offsets (the high word is
+                // one constant) and ring positions are counters rather than divisions.
+                const uint32_t dhi = smem_desc_hi();
+                constexpr uint32_t kStageLo = (2 * L::kQBytes) >> 4, kDsLo = (2 * L::kDsBytes) >> 4;
+                const uint32_t q_lo0 = smem_desc_lo_k128(base + L::q);
+                const uint32_t qt_lo0 = smem_desc_lo_mn128(base + L::q + qt_off, kBwdTile * 128);
+                const uint32_t ds_lo0 = smem_desc_lo_k128(base + L::ds);
+                const uint32_t dsmn_lo0 = smem_desc_lo_mn128(base + L::ds, L::kDsBytes);
+                const uint32_t kt_lo = smem_desc_lo_mn128(kt_tile, a_atom);
+                int s = 0, s2 = 0, dsb = 0;  // ring positions of tile m (scores) and m - 1 (gradients)
+                uint32_t qph = 0, dsph = 0;  // their barrier phases
+                uint32_t q_lo = q_lo0, qt_lo = qt_lo0;
+                uint32_t dk_acc = 0;         // the CTA's first dK MMA starts the accumulator
                 // iteration m issues the scores of tile m, then the gradient MMAs of tile m - 1
                 for (int m = 0; m <= n_tiles; ++m) {
                     if (m < n_tiles) {
-                        const int s = m % NST;
-                        if (!mbar_wait(base + L::bar_qfull + 8 * s, (m / NST) & 1, wc, kErrWaitQ)) break;
+                        if (!mbar_wait(base + L::bar_qfull + 8 * s, qph, wc, kErrWaitQ)) break;
                         if (!mbar_wait(base + L::bar_sempty, (m & 1) ^ 1, wc, kErrWaitS)) break;
                         tc_fence_after();
-                        const uint32_t q1s = base + L::q + 2 * s * L::kQBytes;
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t qo = (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32;
-                            tc_mma_bf16_ta(t_s, t_k + kk * 8, smem_desc_k128(q1s + qo), id_s, kk > 0);
+                            const uint32_t qo = ((kk >> 2) * kBwdTile * 128 + (kk & 3) * 32) >> 4;
+                            tc_mma_bf16_ta_w(t_s, t_k + kk * 8, q_lo + qo, dhi, id_s, kk > 0);
                         }
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t qo = (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32;
-                            tc_mma_bf16_ta(t_s + 64, t_k + D / 2 + kk * 8, smem_desc_k128(q1s + L::kQBytes + qo),
-                                           id_s, kk > 0);
+                            const uint32_t qo = (L::kQBytes + (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32) >> 4;
+                            tc_mma_bf16_ta_w(t_s + 64, t_k + D / 2 + kk * 8, q_lo + qo, dhi, id_s, kk > 0);
                         }
                         tc_commit(base + L::bar_sfull);
+                        if (++s == NST) {
+                            s = 0;
+                            qph ^= 1;
+                            q_lo = q_lo0;
+                        } else {
+                            q_lo += kStageLo;
+                        }
                     }
                     if (m > 0) {
-                        const int mm = m - 1, s = mm % NST, dsb = mm % L::kNumDs;
-                        if (!mbar_wait(base + L::bar_dsfull + 8 * dsb, (mm / L::kNumDs) & 1, wc, kErrWaitOther))
-                            break;
+                        if (!mbar_wait(base + L::bar_dsfull + 8 * dsb, dsph, wc, kErrWaitOther)) break;
                         tc_fence_after();
-                        const uint32_t dss = base + L::ds + 2 * dsb * L::kDsBytes;
-                        const uint32_t qts = base + L::q + 2 * s * L::kQBytes + qt_off;
+                        const uint32_t ds_lo = ds_lo0 + (dsb ? kDsLo : 0u);
                         // dK += dS^T Q_t : A = dS^T (K-major over queries), B = Q_t (MN-major); dS = hi + lo
 #pragma unroll
                         for (int part = 0; part < 2; ++part)
 #pragma unroll
                             for (int kk = 0; kk < kBwdTile / 16; ++kk)
-                                tc_mma_bf16(t_dk, smem_desc_k128(dss + part * L::kDsBytes + kk * 32),
-                                            smem_desc_mn128(qts + kk * 16 * 128, kBwdTile * 128), id_dk,
-                                            (mm | kk | part) != 0);
+                                tc_mma_bf16_w(t_dk, ds_lo + ((part * L::kDsBytes + kk * 32) >> 4), dhi,
+                                              qt_lo + ((kk * 16 * 128) >> 4), dhi, id_dk, (kk | part) ? 1u : dk_acc);
+                        dk_acc = 1;
                         if (FUSED) {
                             // [dQ^T_hi | dQ^T_lo] = K_t^T [dS^T_hi | dS^T_lo]: A = K_t (MN-major), B = the
                             // hi and lo tiles as two 64-query atoms of one N = 128 operand, K = 128 keys
-                            if (!mbar_wait(base + L::bar_dqempty, (mm & 1) ^ 1, wc, kErrWaitOther)) break;
+                            if (!mbar_wait(base + L::bar_dqempty, m & 1, wc, kErrWaitOther)) break;
                             tc_fence_after();
+                            const uint32_t dsmn_lo = dsmn_lo0 + (dsb ? kDsLo : 0u);
 #pragma unroll
                             for (int kk = 0; kk < kBlockK / 16; ++kk)
-                                tc_mma_bf16(t_dq, smem_desc_mn128(kt_tile + kk * 16 * 128, a_atom),
-                                            smem_desc_mn128(dss + kk * 16 * 128, L::kDsBytes), id_dq, kk > 0);
+                                tc_mma_bf16_w(t_dq, kt_lo + ((kk * 16 * 128) >> 4), dhi,
+                                              dsmn_lo + ((kk * 16 * 128) >> 4), dhi, id_dq, kk > 0);
                             tc_commit(base + L::bar_dqfull);
                         }
                         tc_commit(base + L::bar_dsempty + 8 * dsb);
-                        tc_commit(base + L::bar_qempty + 8 * s);
+                        tc_commit(base + L::bar_qempty + 8 * s2);
+                        dsph ^= dsb;  // a buffer's phase flips each time it comes round again
+                        dsb ^= 1;
+                        if (++s2 == NST) {
+                            s2 = 0;
+                            qt_lo = qt_lo0;
+                        } else {
+                            qt_lo += kStageLo;
+                        }
                         ++issued;
                     }
                 }

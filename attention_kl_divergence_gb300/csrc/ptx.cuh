@@ -236,6 +236,46 @@ __device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t saddr, uint32_t ato
     return desc;
 }
 
+// The same descriptors as two 32-bit words.  The high word (stride byte
+// offset, version, swizzle) is one constant for every operand above; the low
+// word holds the start address >> 4 and the leading byte offset.  For a
+// 16-byte aligned operand in the first 256 KB of shared memory, an operand
+// `off` bytes further differs only by off >> 4 in the low word, so an issue
+// loop can form each descriptor with one add.
+__device__ __forceinline__ uint32_t smem_desc_hi() {
+    return (1024u >> 4) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint32_t smem_desc_lo_k128(uint32_t saddr) { return ((saddr >> 4) & 0x3FFFu) | (1u << 16); }
+__device__ __forceinline__ uint32_t smem_desc_lo_mn128(uint32_t saddr, uint32_t atom_stride) {
+    return ((saddr >> 4) & 0x3FFFu) | (((atom_stride >> 4) & 0x3FFFu) << 16);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T with the descriptors as (low, high)
+// words.  A constant `accumulate` (an unrolled loop index test) folds away.
+__device__ __forceinline__ void tc_mma_bf16_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                              uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, B as (low, high) words.
+__device__ __forceinline__ void tc_mma_bf16_ta_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D.  a_mn / b_mn mark
 // an operand stored MN-major (transposed) instead of K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn = 0, int b_mn = 0) {
