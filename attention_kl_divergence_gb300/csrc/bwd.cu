@@ -56,6 +56,23 @@ __device__ __forceinline__ float dscore(float z1, float z2, float c, float scale
     }
 }
 
+// dS for two queries of one key, FP32x2: nla = -la, nxb = -xb, gs = g * scale
+// (the softmax scale of both gradient GEMMs applied here once).
+template <int SETTING>
+__device__ __forceinline__ float2 dscore2(float2 z1, float2 z2, float2 cc, float2 sc, float2 nla, float2 nxb,
+                                          float2 gs) {
+    const float2 x1 = __ffma2_rn(z1, cc, nla);
+    const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+    if (SETTING == 1) {
+        const float2 x2 = __ffma2_rn(z2, cc, nxb);
+        const float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+        return __fmul2_rn(gs, __ffma2_rn(p1, make_float2(-1.f, -1.f), p2));  // g s (p2 - p1)
+    } else {
+        const float2 df = __ffma2_rn(z2, make_float2(-1.f, -1.f), z1);  // z1 - z2
+        return __fmul2_rn(__fmul2_rn(gs, p1), __ffma2_rn(df, sc, nxb));  // g s p1 (scale (z1 - z2) - xb)
+    }
+}
+
 // Per-row constants of the recompute, for row `row` (flat into [B*H*Nq]).
 template <int SETTING>
 __device__ __forceinline__ void row_constants(const BwdParams& p, size_t row, bool valid, float& la, float& xb,
@@ -85,8 +102,9 @@ __device__ __forceinline__ void store_ds_chunk(uint32_t tile_hi, uint32_t tile_l
         for (int k = 0; k < 4; ++k) {
             const float a = v[cc * 8 + 2 * k], b = v[cc * 8 + 2 * k + 1];
             hi[k] = pack_bf16(a, b);
-            const float ha = __uint_as_float(hi[k] << 16), hb = __uint_as_float(hi[k] & 0xffff0000u);
-            lo[k] = pack_bf16(a - ha, b - hb);
+            const float2 h = make_float2(__uint_as_float(hi[k] << 16), __uint_as_float(hi[k] & 0xffff0000u));
+            const float2 r = __ffma2_rn(h, make_float2(-1.f, -1.f), make_float2(a, b));  // exact: v - bf16(v)
+            lo[k] = pack_bf16(r.x, r.y);
         }
         const uint32_t off = roff + (((chunk0 + cc) ^ (row & 7)) << 4);
         st_shared_v4(tile_hi + off, hi[0], hi[1], hi[2], hi[3]);
@@ -507,6 +525,8 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
                     tma_load_4d_hint(q2s + c * kBwdTile * 128, &tQ2, fb, c * kSwizzleCols, r0, h, b, keep);
                 }
             }
+            // per query row: -la, -xb and g * scale (the softmax scale of both
+            // gradients is folded into dS, so neither epilogue multiplies)
             float* v = vec + s * 3 * kBwdTile;
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
@@ -514,9 +534,9 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
                 const int i = r0 + r;
                 float la, xb, g;
                 row_constants<SETTING>(p, (static_cast<size_t>(b) * p.H + h) * p.Nq + i, i < p.Nq, la, xb, g);
-                v[r] = la;
-                v[kBwdTile + r] = xb;
-                v[2 * kBwdTile + r] = g;
+                v[r] = -la;
+                v[kBwdTile + r] = -xb;
+                v[2 * kBwdTile + r] = g * p.scale;
             }
             mbar_arrive(fb);
         }
@@ -646,6 +666,7 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
         const int j = n0 + row;  // key index
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const float c = p.scale_log2e;
+        const float2 cc = make_float2(c, c), sc2 = make_float2(p.scale, p.scale);
         const bool key_ok = j < p.Nk;
         bool ok = true;
         for (int m = 0; m < n_tiles; ++m) {
@@ -672,12 +693,16 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
                 const float4 a = v4[e4], x = v4[kBwdTile / 4 + e4], gg = v4[kBwdTile / 2 + e4];
-                const float la[4] = {a.x, a.y, a.z, a.w}, xb[4] = {x.x, x.y, x.z, x.w},
-                            gv[4] = {gg.x, gg.y, gg.z, gg.w};
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int e = 4 * e4 + k;
-                    dsv[e] = dscore<SETTING>(z1[e], z2[e], c, p.scale, la[k], xb[k], gv[k]);
+                for (int k = 0; k < 2; ++k) {
+                    const int e = 4 * e4 + 2 * k;
+                    const float2 nla = k ? make_float2(a.z, a.w) : make_float2(a.x, a.y);
+                    const float2 nxb = k ? make_float2(x.z, x.w) : make_float2(x.x, x.y);
+                    const float2 gs = k ? make_float2(gg.z, gg.w) : make_float2(gg.x, gg.y);
+                    const float2 d = dscore2<SETTING>(make_float2(z1[e], z1[e + 1]), make_float2(z2[e], z2[e + 1]),
+                                                      cc, sc2, nla, nxb, gs);
+                    dsv[e] = d.x;
+                    dsv[e + 1] = d.y;
                 }
             }
             // query i = r0 + e sees key j iff j <= i + diag_off; keys past Nk contribute nothing
@@ -705,7 +730,7 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
                 float v[32];
                 tmem_ld32(tl + 256 + c0, v);
                 tc_wait_ld();
-                if (key_ok) store_grad32(out, c0, v, p.scale, p.grad_bf16 != 0);
+                if (key_ok) store_grad32(out, c0, v, 1.0f, p.grad_bf16 != 0);  // the scale is in dS
             }
         }
     } else if (FUSED) {
@@ -730,12 +755,20 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
                 tmem_ld32(tl + 448, lo);  // lo half, query rows 0-31
                 tc_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v0[e] += lo[e];
+                for (int e = 0; e < 32; e += 2) {
+                    const float2 t = __fadd2_rn(make_float2(v0[e], v0[e + 1]), make_float2(lo[e], lo[e + 1]));
+                    v0[e] = t.x;
+                    v0[e + 1] = t.y;
+                }
                 tmem_ld32(tl + 416, v1);  // hi half, query rows 32-63
                 tmem_ld32(tl + 480, lo);  // lo half, query rows 32-63
                 tc_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v1[e] += lo[e];
+                for (int e = 0; e < 32; e += 2) {
+                    const float2 t = __fadd2_rn(make_float2(v1[e], v1[e + 1]), make_float2(lo[e], lo[e + 1]));
+                    v1[e] = t.x;
+                    v1[e + 1] = t.y;
+                }
             }
             tc_fence_before();
             mbar_arrive(base + L::bar_dqempty);
@@ -744,10 +777,8 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
             if (f < D) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(stage + e * (D * 4) + f * 4), "f"(v0[e] * p.scale)
-                                 : "memory");
-                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(stage + (e + 32) * (D * 4) + f * 4),
-                                 "f"(v1[e] * p.scale)
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(stage + e * (D * 4) + f * 4), "f"(v0[e]) : "memory");
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(stage + (e + 32) * (D * 4) + f * 4), "f"(v1[e])
                                  : "memory");
                 }
             }
