@@ -419,13 +419,19 @@ struct KvSmem {
     static constexpr int bar_dqfull = bar_dsempty + 16;
     static constexpr int bar_dqempty = bar_dqfull + 16;
     static constexpr int bar_done = bar_dqempty + 16;
-    static constexpr int misc = bar_done + 8;
+    static constexpr int bar_drain = bar_done + 8;  // the score issuer's own drain on abort
+    static constexpr int misc = bar_drain + 8;
     static constexpr int total = misc + 16;
     static constexpr int alloc = total;  // no slack: the kernel checks the base is 1024-byte aligned
 };
 
+// Threads of bwd_kv_kernel: 10 warps (TMA, score MMAs, 8 update), 4 dQ
+// epilogue warps when fused, and the gradient-MMA warp last.
+template <bool FUSED>
+__host__ __device__ constexpr int kv_threads() { return FUSED ? 480 : 352; }
+
 template <int D, int NST, int SETTING, bool FUSED>
-__global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
+__global__ void __launch_bounds__(kv_threads<FUSED>(), 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tQ1, const __grid_constant__ CUtensorMap tK1,
                   const __grid_constant__ CUtensorMap tQ2, const __grid_constant__ CUtensorMap tK2,
                   const BwdParams p) {
@@ -444,6 +450,7 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + L::misc);
     float* vec = reinterpret_cast<float*>(gbase + L::vec);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kGradWarp = kv_threads<FUSED>() / 32 - 1;  // issues the gradient MMAs
 
     // head-major: resident CTAs share one head's query tiles through L2; key
     // tile 0 sees the most query rows under a causal mask and comes first
@@ -478,6 +485,7 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
             mbar_init(base + L::bar_dqempty + 8 * s, 128);
         }
         mbar_init(base + L::bar_done, 1);
+        mbar_init(base + L::bar_drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -548,21 +556,19 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA
+        // ------------------------------------------------ score MMAs
+        // Two threads issue the MMAs: this one the scores of tile m, the
+        // gradient warp's first thread the dK / dQ^T MMAs of earlier tiles.  A
+        // thread waiting on a barrier or committing leaves the tensor pipe to
+        // the other's queued work, and neither waits on the other's barriers.
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_bf16_f32(kBlockK, kBwdTile);
-            constexpr uint32_t id_dk = idesc_bf16_f32(kBlockK, D, 0, 1);
-            constexpr uint32_t id_dq = idesc_bf16_f32(128, 2 * kBwdTile, 1, 1);  // M = 128 features (d = 64: padded)
-            // A = K_t^T as 64-feature atoms: the tile's second block, or the zero atom when d = 64
-            const uint32_t a_atom = D == 128 ? kBlockK * 128 : base + L::zero - kt_tile;
-            const uint32_t t_k = tmem, t_s = tmem + 128, t_dk = tmem + 256, t_dq = tmem + 384;
-            int issued = 0;
+            const uint32_t t_k = tmem, t_s = tmem + 128;
             bool started = false;
             // test aid: a wait on a barrier that nothing arrives on before the end
             const bool stalled = p.inject_stall && blockIdx.x == 0 &&
                                  !mbar_wait(base + L::bar_done, 0, wc, kErrWaitOther);
-            bool ok = !stalled && mbar_wait(base + L::bar_k, 0, wc, kErrWaitK);
-            if (ok) {
+            if (!stalled && n_tiles > 0 && mbar_wait(base + L::bar_k, 0, wc, kErrWaitK)) {
                 tc_fence_after();
                 // the CTA's key tiles become the A operand of every score MMA
 #pragma unroll
@@ -572,86 +578,102 @@ __global__ void __launch_bounds__(FUSED ? 448 : 320, 1)
                     tc_cp_128x256b(t_k + D / 2 + kk * 8, smem_desc_k128(base + L::k2 + ko));
                 }
                 started = true;
-                // The update warps share this thread's scheduler and keep it busy while
-                // they form dS, so the issue loop runs as few instructions as it can:
                 // descriptor low words advance by compile-time offsets (the high word is
-                // one constant) and ring positions are counters rather than divisions.
+                // one constant); ring positions are counters rather than divisions
                 const uint32_t dhi = smem_desc_hi();
-                constexpr uint32_t kStageLo = (2 * L::kQBytes) >> 4, kDsLo = (2 * L::kDsBytes) >> 4;
+                constexpr uint32_t kStageLo = (2 * L::kQBytes) >> 4;
                 const uint32_t q_lo0 = smem_desc_lo_k128(base + L::q);
-                const uint32_t qt_lo0 = smem_desc_lo_mn128(base + L::q + qt_off, kBwdTile * 128);
-                const uint32_t ds_lo0 = smem_desc_lo_k128(base + L::ds);
-                const uint32_t dsmn_lo0 = smem_desc_lo_mn128(base + L::ds, L::kDsBytes);
-                const uint32_t kt_lo = smem_desc_lo_mn128(kt_tile, a_atom);
-                int s = 0, s2 = 0, dsb = 0;  // ring positions of tile m (scores) and m - 1 (gradients)
-                uint32_t qph = 0, dsph = 0;  // their barrier phases
-                uint32_t q_lo = q_lo0, qt_lo = qt_lo0;
-                uint32_t dk_acc = 0;         // the CTA's first dK MMA starts the accumulator
-                // iteration m issues the scores of tile m, then the gradient MMAs of tile m - 1
-                for (int m = 0; m <= n_tiles; ++m) {
-                    if (m < n_tiles) {
-                        if (!mbar_wait(base + L::bar_qfull + 8 * s, qph, wc, kErrWaitQ)) break;
-                        if (!mbar_wait(base + L::bar_sempty, (m & 1) ^ 1, wc, kErrWaitS)) break;
-                        tc_fence_after();
+                int s = 0;
+                uint32_t qph = 0, q_lo = q_lo0;
+                for (int m = 0; m < n_tiles; ++m) {
+                    if (!mbar_wait(base + L::bar_qfull + 8 * s, qph, wc, kErrWaitQ)) break;
+                    if (!mbar_wait(base + L::bar_sempty, (m & 1) ^ 1, wc, kErrWaitS)) break;
+                    tc_fence_after();
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t qo = ((kk >> 2) * kBwdTile * 128 + (kk & 3) * 32) >> 4;
-                            tc_mma_bf16_ta_w(t_s, t_k + kk * 8, q_lo + qo, dhi, id_s, kk > 0);
-                        }
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t qo = (L::kQBytes + (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32) >> 4;
-                            tc_mma_bf16_ta_w(t_s + 64, t_k + D / 2 + kk * 8, q_lo + qo, dhi, id_s, kk > 0);
-                        }
-                        tc_commit(base + L::bar_sfull);
-                        if (++s == NST) {
-                            s = 0;
-                            qph ^= 1;
-                            q_lo = q_lo0;
-                        } else {
-                            q_lo += kStageLo;
-                        }
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t qo = ((kk >> 2) * kBwdTile * 128 + (kk & 3) * 32) >> 4;
+                        tc_mma_bf16_ta_w(t_s, t_k + kk * 8, q_lo + qo, dhi, id_s, kk > 0);
                     }
-                    if (m > 0) {
-                        if (!mbar_wait(base + L::bar_dsfull + 8 * dsb, dsph, wc, kErrWaitOther)) break;
-                        tc_fence_after();
-                        const uint32_t ds_lo = ds_lo0 + (dsb ? kDsLo : 0u);
-                        // dK += dS^T Q_t : A = dS^T (K-major over queries), B = Q_t (MN-major); dS = hi + lo
 #pragma unroll
-                        for (int part = 0; part < 2; ++part)
-#pragma unroll
-                            for (int kk = 0; kk < kBwdTile / 16; ++kk)
-                                tc_mma_bf16_w(t_dk, ds_lo + ((part * L::kDsBytes + kk * 32) >> 4), dhi,
-                                              qt_lo + ((kk * 16 * 128) >> 4), dhi, id_dk, (kk | part) ? 1u : dk_acc);
-                        dk_acc = 1;
-                        if (FUSED) {
-                            // [dQ^T_hi | dQ^T_lo] = K_t^T [dS^T_hi | dS^T_lo]: A = K_t (MN-major), B = the
-                            // hi and lo tiles as two 64-query atoms of one N = 128 operand, K = 128 keys
-                            if (!mbar_wait(base + L::bar_dqempty, m & 1, wc, kErrWaitOther)) break;
-                            tc_fence_after();
-                            const uint32_t dsmn_lo = dsmn_lo0 + (dsb ? kDsLo : 0u);
-#pragma unroll
-                            for (int kk = 0; kk < kBlockK / 16; ++kk)
-                                tc_mma_bf16_w(t_dq, kt_lo + ((kk * 16 * 128) >> 4), dhi,
-                                              dsmn_lo + ((kk * 16 * 128) >> 4), dhi, id_dq, kk > 0);
-                            tc_commit(base + L::bar_dqfull);
-                        }
-                        tc_commit(base + L::bar_dsempty + 8 * dsb);
-                        tc_commit(base + L::bar_qempty + 8 * s2);
-                        dsph ^= dsb;  // a buffer's phase flips each time it comes round again
-                        dsb ^= 1;
-                        if (++s2 == NST) {
-                            s2 = 0;
-                            qt_lo = qt_lo0;
-                        } else {
-                            qt_lo += kStageLo;
-                        }
-                        ++issued;
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t qo = (L::kQBytes + (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32) >> 4;
+                        tc_mma_bf16_ta_w(t_s + 64, t_k + D / 2 + kk * 8, q_lo + qo, dhi, id_s, kk > 0);
                     }
+                    tc_commit(base + L::bar_sfull);
+                    if (++s == NST) {
+                        s = 0;
+                        qph ^= 1;
+                        q_lo = q_lo0;
+                    } else {
+                        q_lo += kStageLo;
+                    }
+                }
+            }
+            if (*abort_flag && started) {  // let the issued copies and MMAs retire before TMEM is freed
+                tc_commit(base + L::bar_drain);
+                drain_wait_b(base + L::bar_drain, 0, kDrainNs);
+            }
+        }
+    } else if (warp == kGradWarp) {
+        // ------------------------------------------------ gradient MMAs
+        // tile m's dS (from the update warps) -> dK += dS^T Q_t, and when fused
+        // [dQ^T_hi | dQ^T_lo] = K_t^T [dS^T_hi | dS^T_lo]; then the tile's dS buffer
+        // and query stage are released.  (Tile m's scores finished before its dS
+        // existed, so these commits also cover the score MMAs that read the stage.)
+        if (lane == 0) {
+            constexpr uint32_t id_dk = idesc_bf16_f32(kBlockK, D, 0, 1);
+            constexpr uint32_t id_dq = idesc_bf16_f32(128, 2 * kBwdTile, 1, 1);  // M = 128 features (d = 64: padded)
+            // A = K_t^T as 64-feature atoms: the tile's second block, or the zero atom when d = 64
+            const uint32_t a_atom = D == 128 ? kBlockK * 128 : base + L::zero - kt_tile;
+            const uint32_t t_dk = tmem + 256, t_dq = tmem + 384;
+            const uint32_t dhi = smem_desc_hi();
+            constexpr uint32_t kStageLo = (2 * L::kQBytes) >> 4, kDsLo = (2 * L::kDsBytes) >> 4;
+            const uint32_t qt_lo0 = smem_desc_lo_mn128(base + L::q + qt_off, kBwdTile * 128);
+            const uint32_t ds_lo0 = smem_desc_lo_k128(base + L::ds);
+            const uint32_t dsmn_lo0 = smem_desc_lo_mn128(base + L::ds, L::kDsBytes);
+            const uint32_t kt_lo = smem_desc_lo_mn128(kt_tile, a_atom);
+            int issued = 0, s2 = 0, dsb = 0;
+            uint32_t dsph = 0, qt_lo = qt_lo0;
+            // the key tiles (A of dQ^T) have landed before any dS exists; the wait states it
+            if (mbar_wait(base + L::bar_k, 0, wc, kErrWaitK)) {
+                for (int m = 0; m < n_tiles; ++m) {
+                    if (!mbar_wait(base + L::bar_dsfull + 8 * dsb, dsph, wc, kErrWaitOther)) break;
+                    tc_fence_after();
+                    const uint32_t ds_lo = ds_lo0 + (dsb ? kDsLo : 0u);
+                    // dK += dS^T Q_t : A = dS^T (K-major over queries), B = Q_t (MN-major); dS = hi + lo
+#pragma unroll
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int kk = 0; kk < kBwdTile / 16; ++kk)
+                            tc_mma_bf16_w(t_dk, ds_lo + ((part * L::kDsBytes + kk * 32) >> 4), dhi,
+                                          qt_lo + ((kk * 16 * 128) >> 4), dhi, id_dk, (kk | part | m) != 0);
+                    if (FUSED) {
+                        // A = K_t (MN-major), B = the hi and lo tiles as two 64-query atoms of one
+                        // N = 128 operand, K = 128 keys
+                        if (!mbar_wait(base + L::bar_dqempty, (m & 1) ^ 1, wc, kErrWaitOther)) break;
+                        tc_fence_after();
+                        const uint32_t dsmn_lo = dsmn_lo0 + (dsb ? kDsLo : 0u);
+#pragma unroll
+                        for (int kk = 0; kk < kBlockK / 16; ++kk)
+                            tc_mma_bf16_w(t_dq, kt_lo + ((kk * 16 * 128) >> 4), dhi, dsmn_lo + ((kk * 16 * 128) >> 4),
+                                          dhi, id_dq, kk > 0);
+                        tc_commit(base + L::bar_dqfull);
+                    }
+                    tc_commit(base + L::bar_dsempty + 8 * dsb);
+                    tc_commit(base + L::bar_qempty + 8 * s2);
+                    dsph ^= dsb;  // a buffer's phase flips each time it comes round again
+                    dsb ^= 1;
+                    if (++s2 == NST) {
+                        s2 = 0;
+                        qt_lo = qt_lo0;
+                    } else {
+                        qt_lo += kStageLo;
+                    }
+                    ++issued;
                 }
                 if (issued == n_tiles) tc_commit(base + L::bar_done);
             }
-            if (*abort_flag && started) {  // let the issued copies and MMAs retire before TMEM is freed
+            if (*abort_flag && issued > 0) {  // let the issued MMAs retire before TMEM is freed
                 tc_commit(base + L::bar_done);
                 drain_wait_b(base + L::bar_done, 0, kDrainNs);
             }
@@ -836,7 +858,7 @@ cudaError_t launch_kv_impl(const CUtensorMap* maps, const BwdParams& p, int ctas
     auto k = bwd_kv_kernel<D, NST, SETTING, FUSED>;
     cudaError_t e = set_smem(k, KvSmem<D, NST>::alloc);
     if (e != cudaSuccess) return e;
-    k<<<ctas, FUSED ? 448 : 320, KvSmem<D, NST>::alloc, st>>>(maps[0], maps[1], maps[2], maps[3], p);
+    k<<<ctas, kv_threads<FUSED>(), KvSmem<D, NST>::alloc, st>>>(maps[0], maps[1], maps[2], maps[3], p);
     return cudaGetLastError();
 }
 
