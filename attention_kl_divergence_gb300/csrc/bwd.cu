@@ -397,28 +397,38 @@ __global__ void __launch_bounds__(320, 1)
 template <int D, int NST>
 struct KvSmem {
     static constexpr int kKBytes = kBlockK * D * 2;    // 128 keys
-    static constexpr int kQBytes = kBwdTile * D * 2;   // 64 query rows
+    static constexpr int kQBytes = kBwdTile * D * 2;   // 64 query rows of one tensor
     static constexpr int kDsBytes = kBlockK * kBwdTile * 2;
+    // Three rings: the trainable side's query tiles (read by the score and the
+    // dK MMAs, so freed after dK), the other side's (read by the score MMAs
+    // only, so freed right after them: half as deep does), and the per-row
+    // constants (freed once the update warps have read them).
+    static constexpr int kQt = NST, kQn = NST / 2, kNv = NST >= 8 ? 4 : 3;
     static constexpr int k1 = 0;
     static constexpr int k2 = kKBytes;
-    static constexpr int q = 2 * kKBytes;
+    static constexpr int qt = 2 * kKBytes;
+    static constexpr int qn = qt + kQt * kQBytes;
     static constexpr int kNumDs = 2;                   // dS buffers (hi + lo each)
-    static constexpr int ds = q + 2 * NST * kQBytes;   // buffer b: hi at ds + 2*b*kDsBytes, lo right after
+    static constexpr int ds = qn + kQn * kQBytes;      // buffer b: hi at ds + 2*b*kDsBytes, lo right after
     // d = 64: a zero 64-feature atom pads the dQ^T MMA's A operand (K_t^T) to M = 128
     static constexpr int zero = ds + 2 * kNumDs * kDsBytes;
     static constexpr int kZeroBytes = D < 128 ? kBlockK * 128 : 0;
-    static constexpr int vec = zero + kZeroBytes;  // [NST][3][64] floats
-    static constexpr int bars = vec + NST * 3 * kBwdTile * 4;
+    static constexpr int vec = zero + kZeroBytes;  // [kNv][3][64] floats
+    static constexpr int bars = vec + kNv * 3 * kBwdTile * 4;
     static constexpr int bar_k = bars;
-    static constexpr int bar_qfull = bar_k + 8;
-    static constexpr int bar_qempty = bar_qfull + 8 * NST;
-    static constexpr int bar_sfull = bar_qempty + 8 * NST;
-    static constexpr int bar_sempty = bar_sfull + 16;
-    static constexpr int bar_dsfull = bar_sempty + 16;
-    static constexpr int bar_dsempty = bar_dsfull + 16;
-    static constexpr int bar_dqfull = bar_dsempty + 16;
-    static constexpr int bar_dqempty = bar_dqfull + 16;
-    static constexpr int bar_done = bar_dqempty + 16;
+    static constexpr int bar_qtfull = bar_k + 8;
+    static constexpr int bar_qtempty = bar_qtfull + 8 * kQt;
+    static constexpr int bar_qnfull = bar_qtempty + 8 * kQt;
+    static constexpr int bar_qnempty = bar_qnfull + 8 * kQn;
+    static constexpr int bar_vfull = bar_qnempty + 8 * kQn;
+    static constexpr int bar_vempty = bar_vfull + 8 * kNv;
+    static constexpr int bar_sfull = bar_vempty + 8 * kNv;
+    static constexpr int bar_sempty = bar_sfull + 8;
+    static constexpr int bar_dsfull = bar_sempty + 8;
+    static constexpr int bar_dsempty = bar_dsfull + 8 * kNumDs;
+    static constexpr int bar_dqfull = bar_dsempty + 8 * kNumDs;
+    static constexpr int bar_dqempty = bar_dqfull + 8;
+    static constexpr int bar_done = bar_dqempty + 8;
     static constexpr int bar_drain = bar_done + 8;  // the score issuer's own drain on abort
     static constexpr int misc = bar_drain + 8;
     static constexpr int total = misc + 16;
@@ -468,22 +478,29 @@ __global__ void __launch_bounds__(kv_threads<FUSED>(), 1)
     auto qhead = [&](int m) { return p.kv_group == 1 ? hk : hk * p.kv_group + m / per_head; };
     auto qtile = [&](int m) { return m_start + (p.kv_group == 1 ? m : m % per_head); };
     const uint32_t kt_tile = base + (SETTING == 1 ? L::k2 : L::k1);  // trainable keys
-    const uint32_t qt_off = SETTING == 1 ? L::kQBytes : 0;           // trainable queries within a stage
 
     if (threadIdx.x == 0) {
         mbar_init(base + L::bar_k, 1);
-        for (int s = 0; s < NST; ++s) {
-            mbar_init(base + L::bar_qfull + 8 * s, 33);
-            mbar_init(base + L::bar_qempty + 8 * s, 1);
+        for (int s = 0; s < L::kQt; ++s) {
+            mbar_init(base + L::bar_qtfull + 8 * s, 1);
+            mbar_init(base + L::bar_qtempty + 8 * s, 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(base + L::bar_sfull + 8 * s, 1);
-            mbar_init(base + L::bar_sempty + 8 * s, 256);
+        for (int s = 0; s < L::kQn; ++s) {
+            mbar_init(base + L::bar_qnfull + 8 * s, 1);
+            mbar_init(base + L::bar_qnempty + 8 * s, 1);
+        }
+        for (int s = 0; s < L::kNv; ++s) {
+            mbar_init(base + L::bar_vfull + 8 * s, 32);
+            mbar_init(base + L::bar_vempty + 8 * s, 256);
+        }
+        for (int s = 0; s < L::kNumDs; ++s) {
             mbar_init(base + L::bar_dsfull + 8 * s, 256);
             mbar_init(base + L::bar_dsempty + 8 * s, 1);
-            mbar_init(base + L::bar_dqfull + 8 * s, 1);
-            mbar_init(base + L::bar_dqempty + 8 * s, 128);
         }
+        mbar_init(base + L::bar_sfull, 1);
+        mbar_init(base + L::bar_sempty, 256);
+        mbar_init(base + L::bar_dqfull, 1);
+        mbar_init(base + L::bar_dqempty, 128);
         mbar_init(base + L::bar_done, 1);
         mbar_init(base + L::bar_drain, 1);
         *abort_flag = 0;
@@ -517,25 +534,36 @@ __global__ void __launch_bounds__(kv_threads<FUSED>(), 1)
             }
         }
         const uint64_t keep = policy_evict_last();
-        int m = 0;
-        for (; m < n_tiles; ++m) {
-            const int s = m % NST;
-            if (!wait_all(base + L::bar_qempty + 8 * s, ((m / NST) & 1) ^ 1, wc, kErrWaitOther)) break;
+        const CUtensorMap* tqt = SETTING == 1 ? &tQ2 : &tQ1;  // the trainable side's queries
+        const CUtensorMap* tqn = SETTING == 1 ? &tQ1 : &tQ2;
+        int n_qt = 0, n_qn = 0;  // tiles whose copies were issued, per ring
+        int st = 0, sn = 0, sv = 0;
+        uint32_t pt = 0, pn = 0, pv = 0;
+        for (int m = 0; m < n_tiles; ++m) {
             const int r0 = qtile(m) * kBwdTile;
             const int h = qhead(m);
-            const uint32_t fb = base + L::bar_qfull + 8 * s;
+            if (!wait_all(base + L::bar_qtempty + 8 * st, pt ^ 1, wc, kErrWaitOther)) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(fb, 2 * L::kQBytes);
-                const uint32_t q1s = base + L::q + 2 * s * L::kQBytes, q2s = q1s + L::kQBytes;
+                const uint32_t fb = base + L::bar_qtfull + 8 * st, dst = base + L::qt + st * L::kQBytes;
+                mbar_arrive_expect_tx(fb, L::kQBytes);
 #pragma unroll
-                for (int c = 0; c < D / kSwizzleCols; ++c) {
-                    tma_load_4d_hint(q1s + c * kBwdTile * 128, &tQ1, fb, c * kSwizzleCols, r0, h, b, keep);
-                    tma_load_4d_hint(q2s + c * kBwdTile * 128, &tQ2, fb, c * kSwizzleCols, r0, h, b, keep);
-                }
+                for (int c = 0; c < D / kSwizzleCols; ++c)
+                    tma_load_4d_hint(dst + c * kBwdTile * 128, tqt, fb, c * kSwizzleCols, r0, h, b, keep);
             }
+            ++n_qt;
+            if (!wait_all(base + L::bar_qnempty + 8 * sn, pn ^ 1, wc, kErrWaitOther)) break;
+            if (lane == 0) {
+                const uint32_t fb = base + L::bar_qnfull + 8 * sn, dst = base + L::qn + sn * L::kQBytes;
+                mbar_arrive_expect_tx(fb, L::kQBytes);
+#pragma unroll
+                for (int c = 0; c < D / kSwizzleCols; ++c)
+                    tma_load_4d_hint(dst + c * kBwdTile * 128, tqn, fb, c * kSwizzleCols, r0, h, b, keep);
+            }
+            ++n_qn;
+            if (!wait_all(base + L::bar_vempty + 8 * sv, pv ^ 1, wc, kErrWaitOther)) break;
             // per query row: -la, -xb and g * scale (the softmax scale of both
             // gradients is folded into dS, so neither epilogue multiplies)
-            float* v = vec + s * 3 * kBwdTile;
+            float* v = vec + sv * 3 * kBwdTile;
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const int r = lane + 32 * k;
@@ -546,13 +574,22 @@ __global__ void __launch_bounds__(kv_threads<FUSED>(), 1)
                 v[kBwdTile + r] = -xb;
                 v[2 * kBwdTile + r] = g * p.scale;
             }
-            mbar_arrive(fb);
+            mbar_arrive(base + L::bar_vfull + 8 * sv);
+            if (++st == L::kQt) st = 0, pt ^= 1;
+            if (++sn == L::kQn) sn = 0, pn ^= 1;
+            if (++sv == L::kNv) sv = 0, pv ^= 1;
         }
-        if (lane == 0) {
-            drain_wait_b(base + L::bar_k, 0, kDrainNs);  // the key tiles' copies have landed
-            for (int j = max(0, m - NST); j < m; ++j) {
-                drain_wait_b(base + L::bar_qfull + 8 * (j % NST), (j / NST) & 1, kDrainNs);
-                if (!*abort_flag) drain_wait_b(base + L::bar_qempty + 8 * (j % NST), (j / NST) & 1, kDrainNs);
+        if (lane == 0) {  // every issued copy has landed (and, unless aborting, been consumed)
+            drain_wait_b(base + L::bar_k, 0, kDrainNs);
+            for (int j = max(0, n_qt - L::kQt); j < n_qt; ++j) {
+                const uint32_t bo = 8 * (j % L::kQt), ph = (j / L::kQt) & 1;
+                drain_wait_b(base + L::bar_qtfull + bo, ph, kDrainNs);
+                if (!*abort_flag) drain_wait_b(base + L::bar_qtempty + bo, ph, kDrainNs);
+            }
+            for (int j = max(0, n_qn - L::kQn); j < n_qn; ++j) {
+                const uint32_t bo = 8 * (j % L::kQn), ph = (j / L::kQn) & 1;
+                drain_wait_b(base + L::bar_qnfull + bo, ph, kDrainNs);
+                if (!*abort_flag) drain_wait_b(base + L::bar_qnempty + bo, ph, kDrainNs);
             }
         }
     } else if (warp == 1) {
@@ -581,31 +618,41 @@ __global__ void __launch_bounds__(kv_threads<FUSED>(), 1)
                 // descriptor low words advance by compile-time offsets (the high word is
                 // one constant); ring positions are counters rather than divisions
                 const uint32_t dhi = smem_desc_hi();
-                constexpr uint32_t kStageLo = (2 * L::kQBytes) >> 4;
-                const uint32_t q_lo0 = smem_desc_lo_k128(base + L::q);
-                int s = 0;
-                uint32_t qph = 0, q_lo = q_lo0;
+                constexpr uint32_t kSlotLo = L::kQBytes >> 4;
+                const uint32_t qt_lo0 = smem_desc_lo_k128(base + L::qt), qn_lo0 = smem_desc_lo_k128(base + L::qn);
+                int st = 0, sn = 0;
+                uint32_t pt = 0, pn = 0, qt_lo = qt_lo0, qn_lo = qn_lo0;
                 for (int m = 0; m < n_tiles; ++m) {
-                    if (!mbar_wait(base + L::bar_qfull + 8 * s, qph, wc, kErrWaitQ)) break;
+                    if (!mbar_wait(base + L::bar_qtfull + 8 * st, pt, wc, kErrWaitQ)) break;
+                    if (!mbar_wait(base + L::bar_qnfull + 8 * sn, pn, wc, kErrWaitQ)) break;
                     if (!mbar_wait(base + L::bar_sempty, (m & 1) ^ 1, wc, kErrWaitS)) break;
                     tc_fence_after();
+                    const uint32_t q1_lo = SETTING == 1 ? qn_lo : qt_lo, q2_lo = SETTING == 1 ? qt_lo : qn_lo;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t qo = ((kk >> 2) * kBwdTile * 128 + (kk & 3) * 32) >> 4;
-                        tc_mma_bf16_ta_w(t_s, t_k + kk * 8, q_lo + qo, dhi, id_s, kk > 0);
+                        tc_mma_bf16_ta_w(t_s, t_k + kk * 8, q1_lo + qo, dhi, id_s, kk > 0);
                     }
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t qo = (L::kQBytes + (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32) >> 4;
-                        tc_mma_bf16_ta_w(t_s + 64, t_k + D / 2 + kk * 8, q_lo + qo, dhi, id_s, kk > 0);
+                        const uint32_t qo = ((kk >> 2) * kBwdTile * 128 + (kk & 3) * 32) >> 4;
+                        tc_mma_bf16_ta_w(t_s + 64, t_k + D / 2 + kk * 8, q2_lo + qo, dhi, id_s, kk > 0);
                     }
                     tc_commit(base + L::bar_sfull);
-                    if (++s == NST) {
-                        s = 0;
-                        qph ^= 1;
-                        q_lo = q_lo0;
+                    tc_commit(base + L::bar_qnempty + 8 * sn);  // the other side's tile is done with
+                    if (++st == L::kQt) {
+                        st = 0;
+                        pt ^= 1;
+                        qt_lo = qt_lo0;
                     } else {
-                        q_lo += kStageLo;
+                        qt_lo += kSlotLo;
+                    }
+                    if (++sn == L::kQn) {
+                        sn = 0;
+                        pn ^= 1;
+                        qn_lo = qn_lo0;
+                    } else {
+                        qn_lo += kSlotLo;
                     }
                 }
             }
@@ -627,8 +674,8 @@ __global__ void __launch_bounds__(kv_threads<FUSED>(), 1)
             const uint32_t a_atom = D == 128 ? kBlockK * 128 : base + L::zero - kt_tile;
             const uint32_t t_dk = tmem + 256, t_dq = tmem + 384;
             const uint32_t dhi = smem_desc_hi();
-            constexpr uint32_t kStageLo = (2 * L::kQBytes) >> 4, kDsLo = (2 * L::kDsBytes) >> 4;
-            const uint32_t qt_lo0 = smem_desc_lo_mn128(base + L::q + qt_off, kBwdTile * 128);
+            constexpr uint32_t kSlotLo = L::kQBytes >> 4, kDsLo = (2 * L::kDsBytes) >> 4;
+            const uint32_t qt_lo0 = smem_desc_lo_mn128(base + L::qt, kBwdTile * 128);
             const uint32_t ds_lo0 = smem_desc_lo_k128(base + L::ds);
             const uint32_t dsmn_lo0 = smem_desc_lo_mn128(base + L::ds, L::kDsBytes);
             const uint32_t kt_lo = smem_desc_lo_mn128(kt_tile, a_atom);
@@ -660,14 +707,18 @@ __global__ void __launch_bounds__(kv_threads<FUSED>(), 1)
                         tc_commit(base + L::bar_dqfull);
                     }
                     tc_commit(base + L::bar_dsempty + 8 * dsb);
-                    tc_commit(base + L::bar_qempty + 8 * s2);
-                    dsph ^= dsb;  // a buffer's phase flips each time it comes round again
-                    dsb ^= 1;
-                    if (++s2 == NST) {
+                    tc_commit(base + L::bar_qtempty + 8 * s2);
+                    if (L::kNumDs == 1) {
+                        dsph ^= 1;
+                    } else {
+                        dsph ^= dsb;  // a buffer's phase flips each time it comes round again
+                        dsb ^= 1;
+                    }
+                    if (++s2 == L::kQt) {
                         s2 = 0;
                         qt_lo = qt_lo0;
                     } else {
-                        qt_lo += kStageLo;
+                        qt_lo += kSlotLo;
                     }
                     ++issued;
                 }
@@ -692,9 +743,9 @@ __global__ void __launch_bounds__(kv_threads<FUSED>(), 1)
         const bool key_ok = j < p.Nk;
         bool ok = true;
         for (int m = 0; m < n_tiles; ++m) {
-            const int s = m % NST;
+            const int sv = m % L::kNv;
             if (!wait_all(base + L::bar_sfull, m & 1, wc, kErrWaitS) ||
-                !wait_all(base + L::bar_qfull + 8 * s, (m / NST) & 1, wc, kErrWaitQ)) {
+                !wait_all(base + L::bar_vfull + 8 * sv, (m / L::kNv) & 1, wc, kErrWaitQ)) {
                 ok = false;
                 break;
             }
@@ -710,7 +761,7 @@ __global__ void __launch_bounds__(kv_threads<FUSED>(), 1)
             tc_fence_before();
             mbar_arrive(base + L::bar_sempty);  // the next score tile may overwrite S now
             // per-query constants of this chunk: 128-bit broadcast loads
-            const float4* v4 = reinterpret_cast<const float4*>(vec + s * 3 * kBwdTile + wg * 32);
+            const float4* v4 = reinterpret_cast<const float4*>(vec + sv * 3 * kBwdTile + wg * 32);
             float dsv[32];
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
@@ -727,6 +778,7 @@ __global__ void __launch_bounds__(kv_threads<FUSED>(), 1)
                     dsv[e + 1] = d.y;
                 }
             }
+            mbar_arrive(base + L::bar_vempty + 8 * sv);  // this tile's row constants are read
             // query i = r0 + e sees key j iff j <= i + diag_off; keys past Nk contribute nothing
             const int first = p.causal ? (j - p.diag_off) - r0 : -1;
             if (first > 0 || !key_ok) {
@@ -853,7 +905,7 @@ cudaError_t launch_q_impl(const CUtensorMap* maps, const BwdParams& p, int ctas,
 
 template <int D, int SETTING, bool FUSED>
 cudaError_t launch_kv_impl(const CUtensorMap* maps, const BwdParams& p, int ctas, cudaStream_t st) {
-    constexpr int NST = D == 128 ? 3 : 6;
+    constexpr int NST = D == 128 ? 4 : 8;  // trainable-side query ring; the other side's is half as deep
     static_assert(KvSmem<D, NST>::alloc <= 232448, "shared memory");
     auto k = bwd_kv_kernel<D, NST, SETTING, FUSED>;
     cudaError_t e = set_smem(k, KvSmem<D, NST>::alloc);
