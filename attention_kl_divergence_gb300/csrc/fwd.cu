@@ -272,28 +272,44 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                                  !mbar_wait(base + L::bar_done, 0, wc, kErrWaitOther);
             if (!stalled && mbar_wait(base + L::bar_q, 0, wc, kErrWaitQ)) {
                 tc_fence_after();
+                // The update warpgroups share this thread's scheduler and keep it busy,
+                // so the issue loop runs few instructions: descriptor low words advance
+                // by compile-time offsets (the high word is one constant) and ring
+                // positions are counters rather than divisions.
+                const uint32_t dhi = smem_desc_hi();
+                const uint32_t q1_lo = smem_desc_lo_k128(base + L::q1), q2_lo = smem_desc_lo_k128(base + L::q2);
+                const uint32_t k_lo0 = smem_desc_lo_k128(base + L::k);
+                constexpr uint32_t kStageLo = (2 * L::kKBytes) >> 4, kK2Lo = L::kKBytes >> 4;
+                int s = 0;
+                uint32_t kph = 0, k_lo = k_lo0;
                 for (int it = 0; it < n_tiles; ++it) {
-                    const int s = it % NST, buf = it & 1;
-                    if (!mbar_wait(base + L::bar_kfull + 8 * s, (it / NST) & 1, wc, kErrWaitK)) break;
+                    const int buf = it & 1;
+                    if (!mbar_wait(base + L::bar_kfull + 8 * s, kph, wc, kErrWaitK)) break;
                     if (!mbar_wait(base + L::bar_sempty + 8 * buf, ((it >> 1) & 1) ^ 1, wc, kErrWaitS)) break;
                     tc_fence_after();
                     const uint32_t d1 = tmem + buf * 2 * kBlockK, d2 = d1 + kBlockK;
-                    const uint32_t k1s = base + L::k + 2 * s * L::kKBytes, k2s = k1s + L::kKBytes;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t qo = (kk >> 2) * kBlockQ * 128 + (kk & 3) * 32;
-                        const uint32_t ko = (kk >> 2) * kBlockK * 128 + (kk & 3) * 32;
-                        tc_mma_bf16(d1, smem_desc_k128(base + L::q1 + qo), smem_desc_k128(k1s + ko), idesc, kk > 0);
+                        const uint32_t qo = ((kk >> 2) * kBlockQ * 128 + (kk & 3) * 32) >> 4;
+                        const uint32_t ko = ((kk >> 2) * kBlockK * 128 + (kk & 3) * 32) >> 4;
+                        tc_mma_bf16_w(d1, q1_lo + qo, dhi, k_lo + ko, dhi, idesc, kk > 0);
                     }
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t qo = (kk >> 2) * kBlockQ * 128 + (kk & 3) * 32;
-                        const uint32_t ko = (kk >> 2) * kBlockK * 128 + (kk & 3) * 32;
-                        tc_mma_bf16(d2, smem_desc_k128(base + L::q2 + qo), smem_desc_k128(k2s + ko), idesc, kk > 0);
+                        const uint32_t qo = ((kk >> 2) * kBlockQ * 128 + (kk & 3) * 32) >> 4;
+                        const uint32_t ko = ((kk >> 2) * kBlockK * 128 + (kk & 3) * 32) >> 4;
+                        tc_mma_bf16_w(d2, q2_lo + qo, dhi, k_lo + kK2Lo + ko, dhi, idesc, kk > 0);
                     }
                     tc_commit(base + L::bar_sfull + 8 * buf);
                     tc_commit(base + L::bar_kempty + 8 * s);
                     ++issued;
+                    if (++s == NST) {
+                        s = 0;
+                        kph ^= 1;
+                        k_lo = k_lo0;
+                    } else {
+                        k_lo += kStageLo;
+                    }
                 }
             }
             if (*abort_flag && issued > 0) {  // let the issued MMAs retire before TMEM is freed
