@@ -27,7 +27,9 @@ constexpr float kTau = 8.0f;  // lazy rescale: tolerate running maxima up to 2^8
 // Update warpgroups of the tile kernel: each takes 128 / (32 * kFwdGroups)
 // 32-column chunks of every score tile and keeps its own running state per row.
 constexpr int kFwdGroups = 2;
-constexpr int kFwdThreads = 64 + 128 * kFwdGroups;
+// warp 0 TMA, warp 1 the S1 MMAs, the update warpgroups, and a last warp for the S2 MMAs
+constexpr int kFwdThreads = 64 + 128 * kFwdGroups + 32;
+constexpr int kFwdS2Warp = kFwdThreads / 32 - 1;
 // Bound of the waits that let in-flight TMA copies and MMAs retire before a CTA
 // exits (independent of the caller's wait limit).
 constexpr uint64_t kDrainNs = 200000000ull;
@@ -48,8 +50,8 @@ struct TileSmem {
     static constexpr int bar_kempty = bar_kfull + 8 * NST;
     static constexpr int bar_sfull = bar_kempty + 8 * NST;
     static constexpr int bar_sempty = bar_sfull + 16;
-    static constexpr int bar_done = bar_sempty + 16;  // drain barrier of an aborted MMA issuer
-    static constexpr int misc = bar_done + 8;     // tmem base (4 B), abort flag (4 B)
+    static constexpr int bar_done = bar_sempty + 16;  // drain barriers of aborted MMA issuers (S1, S2)
+    static constexpr int misc = bar_done + 16;    // tmem base (4 B), abort flag (4 B)
     static constexpr int red = misc + 16;         // [groups - 1][5][128] floats: the other groups' row states
     static constexpr int total = red + (kFwdGroups - 1) * 5 * 128 * 4;
     static constexpr int alloc = total + 1024;    // slack for 1024-byte alignment
@@ -63,19 +65,20 @@ __device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t 
     return true;
 }
 
-// One 32-column chunk of a score row: online update of the five scalars.
+// One W-column piece of a score row: online update of the five scalars.
 // MASKED: only columns e <= last are visible (causal frontier or key tail).
 // The unmasked path (every tile but the diagonal and tail ones) runs on packed
 // FP32x2 arithmetic and three-input maxima.
-template <bool MASKED>
-__device__ __forceinline__ void update_chunk(const float (&z1)[32], const float (&z2)[32], int last, RowState& st,
+template <bool MASKED, int W>
+__device__ __forceinline__ void update_chunk(const float (&z1)[W], const float (&z2)[W], int last, RowState& st,
                                              float c, float tau) {
+    static_assert(W % 4 == 0, "pieces of whole 4-column groups");
     if (MASKED && last < 0) return;  // the whole chunk lies beyond the row's last key
     float cm1, cm2;
     if (MASKED) {
         cm1 = cm2 = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < W; ++e) {
             if (e <= last) {
                 cm1 = fmaxf(cm1, z1[e]);
                 cm2 = fmaxf(cm2, z2[e]);
@@ -84,7 +87,7 @@ __device__ __forceinline__ void update_chunk(const float (&z1)[32], const float 
     } else {
         float a1 = -INFINITY, b1 = -INFINITY, a2 = -INFINITY, b2 = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
+        for (int e = 0; e < W; e += 4) {
             a1 = max3f(a1, z1[e], z1[e + 1]);
             b1 = max3f(b1, z1[e + 2], z1[e + 3]);
             a2 = max3f(a2, z2[e], z2[e + 1]);
@@ -109,7 +112,7 @@ __device__ __forceinline__ void update_chunk(const float (&z1)[32], const float 
     if (MASKED) {
         float s1 = 0.f, s2 = 0.f, sa = 0.f;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < W; ++e) {
             if (e <= last) {
                 const float p1 = ex2(fmaf(z1[e], c, n1));
                 s1 += p1;
@@ -128,7 +131,7 @@ __device__ __forceinline__ void update_chunk(const float (&z1)[32], const float 
     float2 s2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     float2 sa[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) {
+    for (int e = 0; e < W; e += 2) {
         const int k = (e >> 1) & 1;
         const float2 u1 = make_float2(z1[e], z1[e + 1]), u2 = make_float2(z2[e], z2[e + 1]);
         const float2 x1 = __ffma2_rn(u1, cc, nn1);
@@ -208,13 +211,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_init(base + L::bar_q, 1);
         for (int s = 0; s < NST; ++s) {
             mbar_init(base + L::bar_kfull + 8 * s, 1);
-            mbar_init(base + L::bar_kempty + 8 * s, 1);
+            mbar_init(base + L::bar_kempty + 8 * s, 2);  // both issuers' MMAs have read the stage
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(base + L::bar_sfull + 8 * s, 1);
+            mbar_init(base + L::bar_sfull + 8 * s, 2);  // S1 and S2 of the buffer are complete
             mbar_init(base + L::bar_sempty + 8 * s, 128 * kFwdGroups);
         }
         mbar_init(base + L::bar_done, 1);
+        mbar_init(base + L::bar_done + 8, 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -261,25 +265,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 if (!*abort_flag) drain_wait(base + L::bar_kempty + 8 * (j % NST), (j / NST) & 1, kDrainNs);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == kFwdS2Warp) {
         // ------------------------------------------------------------ MMA
+        // Two threads issue the MMAs, S1 = Q1 K1^T (warp 1) and S2 = Q2 K2^T
+        // (the last warp), each committing its own arrival on the shared
+        // barriers: the update warpgroups share their schedulers and keep them
+        // busy, and two issuers keep the tensor pipe fed when one is held up.
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t idesc = idesc_bf16_f32(kBlockQ, kBlockK);
+            const bool second = warp != 1;
+            const uint32_t done_bar = base + L::bar_done + (second ? 8 : 0);
             int issued = 0;
             // test aid: a wait on a barrier that nothing arrives on (bar_done is
             // only committed on the abort path below) gives up after wait_ns
-            const bool stalled = p.inject_stall && blockIdx.x == 0 &&
+            const bool stalled = p.inject_stall && blockIdx.x == 0 && !second &&
                                  !mbar_wait(base + L::bar_done, 0, wc, kErrWaitOther);
             if (!stalled && mbar_wait(base + L::bar_q, 0, wc, kErrWaitQ)) {
                 tc_fence_after();
-                // The update warpgroups share this thread's scheduler and keep it busy,
-                // so the issue loop runs few instructions: descriptor low words advance
-                // by compile-time offsets (the high word is one constant) and ring
-                // positions are counters rather than divisions.
+                // few instructions per MMA: descriptor low words advance by
+                // compile-time offsets (the high word is one constant) and ring
+                // positions are counters rather than divisions
                 const uint32_t dhi = smem_desc_hi();
-                const uint32_t q1_lo = smem_desc_lo_k128(base + L::q1), q2_lo = smem_desc_lo_k128(base + L::q2);
-                const uint32_t k_lo0 = smem_desc_lo_k128(base + L::k);
-                constexpr uint32_t kStageLo = (2 * L::kKBytes) >> 4, kK2Lo = L::kKBytes >> 4;
+                const uint32_t q_lo = smem_desc_lo_k128(base + (second ? L::q2 : L::q1));
+                const uint32_t k_lo0 = smem_desc_lo_k128(base + L::k) + (second ? (L::kKBytes >> 4) : 0u);
+                constexpr uint32_t kStageLo = (2 * L::kKBytes) >> 4;
+                const uint32_t dcol = second ? kBlockK : 0u;
                 int s = 0;
                 uint32_t kph = 0, k_lo = k_lo0;
                 for (int it = 0; it < n_tiles; ++it) {
@@ -287,18 +297,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     if (!mbar_wait(base + L::bar_kfull + 8 * s, kph, wc, kErrWaitK)) break;
                     if (!mbar_wait(base + L::bar_sempty + 8 * buf, ((it >> 1) & 1) ^ 1, wc, kErrWaitS)) break;
                     tc_fence_after();
-                    const uint32_t d1 = tmem + buf * 2 * kBlockK, d2 = d1 + kBlockK;
+                    const uint32_t d = tmem + buf * 2 * kBlockK + dcol;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t qo = ((kk >> 2) * kBlockQ * 128 + (kk & 3) * 32) >> 4;
                         const uint32_t ko = ((kk >> 2) * kBlockK * 128 + (kk & 3) * 32) >> 4;
-                        tc_mma_bf16_w(d1, q1_lo + qo, dhi, k_lo + ko, dhi, idesc, kk > 0);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t qo = ((kk >> 2) * kBlockQ * 128 + (kk & 3) * 32) >> 4;
-                        const uint32_t ko = ((kk >> 2) * kBlockK * 128 + (kk & 3) * 32) >> 4;
-                        tc_mma_bf16_w(d2, q2_lo + qo, dhi, k_lo + kK2Lo + ko, dhi, idesc, kk > 0);
+                        tc_mma_bf16_w(d, q_lo + qo, dhi, k_lo + ko, dhi, idesc, kk > 0);
                     }
                     tc_commit(base + L::bar_sfull + 8 * buf);
                     tc_commit(base + L::bar_kempty + 8 * s);
@@ -313,12 +317,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
             }
             if (*abort_flag && issued > 0) {  // let the issued MMAs retire before TMEM is freed
-                tc_commit(base + L::bar_done);
-                drain_wait(base + L::bar_done, 0, kDrainNs);
+                tc_commit(done_bar);
+                drain_wait(done_bar, 0, kDrainNs);
             }
         }
     } else {
-        // ------------------------------------------------------------ online update
+        // ------------------------------------------------------------ online update (warps 2 .. 2 + 4 groups)
         // kFwdGroups warpgroups split every tile's 128 columns; each keeps its
         // own running state per row, and the states of a row are merged at the
         // end (the same log-sum-exp merge as the Split-K combine).
@@ -355,9 +359,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 }
                 const int last = jrem - ch * 32;
                 if (last >= 31)
-                    update_chunk<false>(z1, z2, 31, st, c, tau);
+                    update_chunk<false, 32>(z1, z2, 31, st, c, tau);
                 else
-                    update_chunk<true>(z1, z2, last, st, c, tau);
+                    update_chunk<true, 32>(z1, z2, last, st, c, tau);
             }
         }
         float* red = reinterpret_cast<float*>(gbase + L::red);
