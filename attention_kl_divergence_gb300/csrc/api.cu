@@ -115,9 +115,12 @@ streamkl_status plan_fwd(const streamkl_shape* s, int causal, const streamkl_opt
 
 struct BwdPlan {
     bool fused;
+    bool keysplit;  // at most 16 query rows per key head: key-split kernel
     bool bf16;
     int ctas_q;
     int ctas_kv;
+    int splits;     // key-split kernel: key-range splits per key head
+    int ctas_dec;
     size_t ws_bytes;
 };
 
@@ -133,16 +136,31 @@ streamkl_status plan_bwd(const streamkl_shape* s, int setting, int causal, const
     if (st != STREAMKL_OK) return st;
     if (setting != 1 && setting != 2) return STREAMKL_ERR_INVALID_ARG;
     const int mode = opt ? opt->bwd_mode : 0;
-    if (mode < 0 || mode > 2) return STREAMKL_ERR_INVALID_ARG;
+    if (mode < 0 || mode > 3) return STREAMKL_ERR_INVALID_ARG;
     if (opt && ((opt->grad_bf16 != 0 && opt->grad_bf16 != 1) || (opt->debug_flags & ~STREAMKL_DEBUG_INJECT_STALL)))
         return STREAMKL_ERR_INVALID_ARG;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
     const int64_t BH = int64_t(s->B) * s->H;
+    // every query row of a key head fits the 16 columns of one CTA: the key-split kernel
+    const bool fits = int64_t(s->Nq) * (s->H / kv_heads(s)) <= kDecodeMaxQ;
+    if (mode == 3 && !fits) return STREAMKL_ERR_UNSUPPORTED;
+    pl->keysplit = mode == 3 || (mode == 0 && fits);
     if (mode == 0)
-        pl->fused = true;
+        pl->fused = !pl->keysplit;
     else
         pl->fused = mode == 1;
+    pl->splits = 1;
+    pl->ctas_dec = 0;
+    if (pl->keysplit) {
+        int sms = 0;
+        if ((st = device_sms(&sms)) != STREAMKL_OK) return st;
+        const int64_t units = int64_t(s->B) * kv_heads(s);
+        const int k_tiles = (s->Nk + kBlockK - 1) / kBlockK;
+        pl->splits = choose_splits(units, k_tiles, sms);
+        if (units * pl->splits > INT32_MAX) return STREAMKL_ERR_UNSUPPORTED;
+        pl->ctas_dec = static_cast<int>(units * pl->splits);
+    }
     const int64_t ctas_kv = int64_t(s->B) * kv_heads(s) * ((s->Nk + kBlockK - 1) / kBlockK);
     const int64_t ctas_q = BH * ((s->Nq + kBlockQ - 1) / kBlockQ);
     if (ctas_kv > INT32_MAX || ctas_q > INT32_MAX) return STREAMKL_ERR_UNSUPPORTED;
@@ -150,8 +168,8 @@ streamkl_status plan_bwd(const streamkl_shape* s, int setting, int causal, const
     pl->ctas_q = static_cast<int>(ctas_q);
     pl->bf16 = opt && opt->grad_bf16 == 1;
     pl->ws_bytes = kStatusBytes;
-    // bf16 gradients from the fused mode: dQ is accumulated in float32 in the workspace first
-    if (pl->fused && pl->bf16) pl->ws_bytes += size_t(BH) * s->Nq * s->d * sizeof(float);
+    // bf16 gradients from a mode that adds dQ up: dQ is accumulated in float32 in the workspace first
+    if ((pl->fused || pl->keysplit) && pl->bf16) pl->ws_bytes += size_t(BH) * s->Nq * s->d * sizeof(float);
     return STREAMKL_OK;
 }
 
@@ -305,10 +323,11 @@ streamkl_status streamkl_bwd_plan(const streamkl_shape* shape, int setting, int 
     BwdPlan pl{};
     streamkl_status st = plan_bwd(shape, setting, causal, opt, &pl);
     if (st != STREAMKL_OK) return st;
-    plan->path = pl.fused ? 2 : 3;
-    plan->num_splits = 1;
-    plan->num_ctas = pl.ctas_kv;
-    plan->launches = (pl.fused && pl.bf16) ? 3 : 2;  // fused: zero dQ + kernel (+ bf16 conversion); split: two kernels
+    plan->path = pl.keysplit ? 4 : pl.fused ? 2 : 3;
+    plan->num_splits = pl.splits;
+    plan->num_ctas = pl.keysplit ? pl.ctas_dec : pl.ctas_kv;
+    // fused and key-split: zero dQ + kernel (+ bf16 conversion); split: two kernels
+    plan->launches = ((pl.fused || pl.keysplit) && pl.bf16) ? 3 : 2;
     plan->workspace_bytes = pl.ws_bytes;
     return STREAMKL_OK;
 }
@@ -351,13 +370,36 @@ streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const flo
     p.dQ = dQ;
     p.dK = dK;
     p.grad_bf16 = pl.bf16 ? 1 : 0;
-    p.dQacc = pl.fused ? (pl.bf16 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes)
-                                  : static_cast<float*>(dQ))
-                       : nullptr;
+    p.dQacc = (pl.fused || pl.keysplit)
+                  ? (pl.bf16 ? reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes)
+                             : static_cast<float*>(dQ))
+                  : nullptr;
     p.status = static_cast<unsigned int*>(workspace);
     p.wait_ns = static_cast<unsigned long long>(wait_limit(opt));
     p.inject_stall = (opt && (opt->debug_flags & STREAMKL_DEBUG_INJECT_STALL)) ? 1 : 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t dq_elems = size_t(shape->B) * shape->H * shape->Nq * shape->d;
+
+    if (pl.keysplit) {
+        // Q boxes: the Nq rows of all kv_group heads of a key head; K boxes of 128 rows
+        CUtensorMap dm[4];
+        if (!make_map(&dm[0], Q1, shape, true, shape->Nq, p.kv_group) ||
+            !make_map(&dm[1], K1, shape, false, kBlockK) ||
+            !make_map(&dm[2], Q2, shape, true, shape->Nq, p.kv_group) || !make_map(&dm[3], K2, shape, false, kBlockK))
+            return STREAMKL_ERR_CUDA;
+        BwdParams pd = p;
+        pd.num_q_tiles = 1;
+        pd.num_k_tiles = (shape->Nk + kBlockK - 1) / kBlockK;
+        pd.num_splits = pl.splits;
+        if (cudaMemsetAsync(p.dQacc, 0, dq_elems * sizeof(float), s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+        if (launch_bwd_decode(shape->d, setting, dm, pd, pl.ctas_dec, s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+        if (pl.bf16) {
+            int sms = 0;
+            if (device_sms(&sms) != STREAMKL_OK) return STREAMKL_ERR_CUDA;
+            if (launch_to_bf16(p.dQacc, dQ, dq_elems, sms, s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+        }
+        return STREAMKL_OK;
+    }
 
     // key-tile kernel: Q boxes of 64 rows, K boxes of 128 rows
     CUtensorMap kv[4];
@@ -368,7 +410,6 @@ streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const flo
     pkv.num_q_tiles = (shape->Nq + 63) / 64;
     pkv.num_k_tiles = (shape->Nk + kBlockK - 1) / kBlockK;
     if (pl.fused) {
-        const size_t dq_elems = size_t(shape->B) * shape->H * shape->Nq * shape->d;
         if (cudaMemsetAsync(p.dQacc, 0, dq_elems * sizeof(float), s) != cudaSuccess) return STREAMKL_ERR_CUDA;
         if (launch_bwd_kv(shape->d, setting, true, kv, pkv, pl.ctas_kv, s) != cudaSuccess) return STREAMKL_ERR_CUDA;
         if (pl.bf16) {

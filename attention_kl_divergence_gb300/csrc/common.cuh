@@ -52,6 +52,7 @@ struct BwdParams {
     int diag_off;        // Nk - Nq
     int H_kv;            // key heads
     int kv_group;        // query heads per key head
+    int num_splits;      // key-split backward: key-range splits per key head
     float scale;
     float scale_log2e;
     const float* g;      // [B*H*Nq] upstream gradient dL/dKL

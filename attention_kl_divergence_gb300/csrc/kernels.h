@@ -21,5 +21,9 @@ cudaError_t launch_bwd_q(int d, int setting, const CUtensorMap* maps, const BwdP
 cudaError_t launch_to_bf16(const float* in, void* out, size_t n, int sms, cudaStream_t stream);
 cudaError_t launch_bwd_kv(int d, int setting, bool fused, const CUtensorMap* maps, const BwdParams& p, int ctas,
                           cudaStream_t stream);
+// Key-split backward for at most 16 query rows per key head: Q maps with boxes
+// of Nq rows x kv_group heads, K maps with 128-row boxes; p.num_splits set.
+cudaError_t launch_bwd_decode(int d, int setting, const CUtensorMap* maps, const BwdParams& p, int ctas,
+                              cudaStream_t stream);
 
 }  // namespace streamkl

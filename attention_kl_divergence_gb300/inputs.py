@@ -45,6 +45,14 @@ class Workload:
         hk = self.H_kv or self.H
         return 2 * 2 * self.B * (self.H * self.Nq + hk * self.Nk) * self.d + 12 * self.B * self.H * self.Nq
 
+    def bwd_bytes(self) -> int:
+        """Algorithmic HBM bytes of one backward with float32 gradients: every Q
+        and K element read once (bf16), LSE1, LSE2, KL and g read (16 B per row),
+        dQ and dK of the trainable side written once (float32)."""
+        hk = self.H_kv or self.H
+        rows_q, rows_k = self.B * self.H * self.Nq, self.B * hk * self.Nk
+        return 2 * 2 * (rows_q + rows_k) * self.d + 16 * rows_q + 4 * (rows_q + rows_k) * self.d
+
     def visible_pairs(self) -> int:
         """Query/key pairs inside the mask, per head.  Causal rows are aligned
         bottom-right (row i sees keys j <= i + Nk - Nq), so row i sees
@@ -70,6 +78,9 @@ WORKLOADS = {
     # decode with keys shared by groups of 4 query heads (32 query heads, 8 key heads)
     "decode_gqa_q1_k128k": Workload("decode_gqa_q1_k128k", 4, 32, 1, 131072, 128, 0.3, False, seed=7,
                                     fwd_only=True, H_kv=8),
+    # backward of a decode-shaped problem: 16 query rows against 128K keys, both settings; each
+    # 128-key tile is its own CTA, so the key range is split across the whole grid
+    "decode_bwd_q16_k128k": Workload("decode_bwd_q16_k128k", 4, 32, 16, 131072, 128, 0.3, False, seed=8),
     # one batch of the 128K decode: small enough for a full ncu capture (2 GiB of keys)
     "decode_q1_k128k_b1": Workload("decode_q1_k128k_b1", 1, 32, 1, 131072, 128, 0.3, False, seed=3,
                                    fwd_only=True),

@@ -22,8 +22,8 @@ import torch
 from . import build as _build
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
-PATH_TILE, PATH_DECODE, PATH_BWD_FUSED, PATH_BWD_SPLIT = range(4)
-BWD_AUTO, BWD_FUSED, BWD_SPLIT = 0, 1, 2
+PATH_TILE, PATH_DECODE, PATH_BWD_FUSED, PATH_BWD_SPLIT, PATH_BWD_KEYSPLIT = range(5)
+BWD_AUTO, BWD_FUSED, BWD_SPLIT, BWD_KEYSPLIT = 0, 1, 2, 3
 
 
 class Shape(ctypes.Structure):

@@ -53,6 +53,9 @@ TRAFFIC = {
 }
 
 
+BWD_MODE_NAMES = {2: "fused", 3: "split", 4: "keysplit"}  # plan paths of the backward
+
+
 def traffic_for(workload, which):
     return TRAFFIC.get((workload, which))
 
@@ -215,9 +218,10 @@ def run_gpu(args):
 
     with_bwd = not w.fwd_only
     launches_per_step = fplan.launches + ((bplan1.launches + bplan2.launches) if with_bwd else 0)
-    if with_bwd and bplan1.path == streamkl.PATH_BWD_FUSED:
+    adds_dq = (streamkl.PATH_BWD_FUSED, streamkl.PATH_BWD_KEYSPLIT)
+    if with_bwd and bplan1.path in adds_dq:
         launches_per_step -= 1  # the dQ zero-fill is a memset, not one of our kernels
-    if with_bwd and bplan2.path == streamkl.PATH_BWD_FUSED:
+    if with_bwd and bplan2.path in adds_dq:
         launches_per_step -= 1
 
     def step():
@@ -267,29 +271,37 @@ def run_gpu(args):
                        peaks["hbm_gbs"], "path": "tile" if fplan.path == 0 else "decode",
                        "splits": fplan.num_splits}}
     if with_bwd:
-        kernels["bwd_setting1"] = {"ms": b1_ms, "tflops": f_bwd / b1_ms / 1e9,
-                                   "frac_bf16_peak": f_bwd / b1_ms / 1e9 / peak_tf,
-                                   "mode": "fused" if bplan1.path == streamkl.PATH_BWD_FUSED else "split"}
-        kernels["bwd_setting2"] = {"ms": b2_ms, "tflops": f_bwd / b2_ms / 1e9,
-                                   "frac_bf16_peak": f_bwd / b2_ms / 1e9 / peak_tf,
-                                   "mode": "fused" if bplan2.path == streamkl.PATH_BWD_FUSED else "split"}
+        for name, ms, plan in (("bwd_setting1", b1_ms, bplan1), ("bwd_setting2", b2_ms, bplan2)):
+            kernels[name] = {"ms": ms, "tflops": f_bwd / ms / 1e9, "frac_bf16_peak": f_bwd / ms / 1e9 / peak_tf,
+                             "gbs": w.bwd_bytes() / ms / 1e6, "frac_hbm_peak": w.bwd_bytes() / ms / 1e6 /
+                             peaks["hbm_gbs"],
+                             "mode": BWD_MODE_NAMES[plan.path]}
     # Roofline of the dominant kernel (largest share of the step), timed live
     # with CUDA events around its call on the launching stream.  Forward call =
     # one fwd_tile_kernel launch (4*d flops per visible pair), or for decode one
     # fwd_decode_kernel + combine launch bounded by HBM (every Q/K byte once);
     # fused backward call = dQ zero-fill + one bwd_kv_kernel launch carrying the
-    # whole backward (8*d flops per visible pair); split = bwd_q + bwd_kv.
+    # whole backward (8*d flops per visible pair); split = bwd_q + bwd_kv;
+    # key-split (at most 16 query rows per key head) = dQ zero-fill + one
+    # bwd_decode_kernel launch, bounded by HBM like the decode forward.
+    def bwd_name(plan, setting):
+        if plan.path == streamkl.PATH_BWD_FUSED:
+            return f"bwd_kv_kernel<setting {setting}, fused>"
+        if plan.path == streamkl.PATH_BWD_KEYSPLIT:
+            return f"bwd_decode_kernel<setting {setting}>"
+        return f"bwd_q_kernel + bwd_kv_kernel (setting {setting})"
+
     names = {"fwd": "fwd_tile_kernel" if fplan.path == 0 else "fwd_decode_kernel + combine_kernel",
-             "bwd_setting1": "bwd_kv_kernel<setting 1, fused>" if bplan1.path == streamkl.PATH_BWD_FUSED
-             else "bwd_q_kernel + bwd_kv_kernel (setting 1)",
-             "bwd_setting2": "bwd_kv_kernel<setting 2, fused>" if bplan2.path == streamkl.PATH_BWD_FUSED
-             else "bwd_q_kernel + bwd_kv_kernel (setting 2)"}
+             "bwd_setting1": bwd_name(bplan1, 1), "bwd_setting2": bwd_name(bplan2, 2)}
     top = max(kernels, key=lambda k: kernels[k]["ms"])
-    if top == "fwd" and fplan.path == streamkl.PATH_DECODE:
-        achieved = w.fwd_bytes() / fwd_ms / 1e6
+    # a decode-shaped problem (at most 16 query rows) moves ~1 (N_Q = 1) to ~16 flops per
+    # byte in either direction, far below the ridge: HBM bounds its kernels
+    if Nq <= 16:
+        nbytes = w.fwd_bytes() if top == "fwd" else w.bwd_bytes()
+        achieved = nbytes / kernels[top]["ms"] / 1e6
         roofline = {"kernel": names[top], "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_for(w.name, top),
-                    "share_of_step": kernels[top]["ms"] / step_ms, "bytes_per_launch": w.fwd_bytes(),
+                    "share_of_step": kernels[top]["ms"] / step_ms, "bytes_per_launch": nbytes,
                     "peak_source": f"hbm_gbs ({peak_src})"}
     else:
         flops_top = f_fwd if top == "fwd" else f_bwd

@@ -84,7 +84,8 @@ typedef struct {
 typedef struct {
     int32_t num_splits;    /* forward: 0 = automatic, n >= 1 forces n key splits     */
     int32_t bwd_mode;      /* backward: 0 = automatic, 1 = fused (atomic dQ),        */
-                           /*           2 = separate dQ and dK kernels                */
+                           /*           2 = separate dQ and dK kernels,               */
+                           /*           3 = key-split (needs Nq * H / H_kv <= 16)     */
     int64_t wait_limit_ns; /* limit of every in-kernel wait; 0 = default (2 s)      */
     int32_t debug_flags;   /* 0 in normal use; see STREAMKL_DEBUG_*                  */
     int32_t grad_bf16;     /* backward: 0 = float32 dQ/dK, 1 = bf16 dQ/dK            */
@@ -99,8 +100,11 @@ typedef struct {
 /* What a call will launch for a given shape (filled by the plan queries). */
 typedef struct {
     int32_t path;       /* 0 = tile forward, 1 = decode (Nq <= 16, causal or not) forward,
-                           2 = fused backward, 3 = separate-kernel backward */
-    int32_t num_splits; /* key splits of the forward (1 = no combine step)  */
+                           2 = fused backward, 3 = separate-kernel backward,
+                           4 = key-split backward (at most 16 query rows per key head;
+                               the automatic choice there) */
+    int32_t num_splits; /* key splits of the forward (1 = no combine step) or of the
+                           key-split backward */
     int32_t num_ctas;   /* CTAs of the main kernel                          */
     int32_t launches;   /* kernels launched per call                        */
     size_t workspace_bytes;

@@ -4,6 +4,7 @@ time are sampled -- first/last rows, tile edges, random rows -- from a few
 heads; the oracle gets exact float64 copies of those heads only.
 
 Workloads (seeded synthetic inputs, see attention_kl_divergence_gb300.inputs):
+  decode-shaped backward, B4 H32 N_Q=16 N_K=128K d128, both settings;
   64K causal and non-causal, B1 H32 d128; decode Split-K, B4 H32 d128,
   N_Q in {1, 16}, N_K in {128K, 512K}; 512K causal, B1 H8 d128, teacher x1.5.
 A key's dK needs every query row that sees it, so dK is sampled among the
@@ -127,3 +128,12 @@ def test_512k_causal_forward_and_setting2():
 
 def test_64k_causal_d64_forward_and_setting1():
     run_workload("64k_causal_d64", (1,), heads=(0, 31), rows_per_head=32, key_tail=512, keys_per_head=16)
+
+
+def test_decode_shaped_backward_both_settings():
+    """16 query rows against 128K keys: every key tile is its own CTA, and all
+    of them add into the same 16 rows of dQ.  dQ is checked on all rows of the
+    sampled heads, dK on keys drawn from the whole key range."""
+    w = WORKLOADS["decode_bwd_q16_k128k"]
+    run_workload(w.name, (1, 2), heads=(0, 77, w.B * w.H - 1), rows_per_head=2 * w.Nq, key_tail=w.Nk,
+                 keys_per_head=32)
