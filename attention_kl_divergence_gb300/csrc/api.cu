@@ -157,7 +157,10 @@ streamkl_status plan_bwd(const streamkl_shape* s, int setting, int causal, const
         if ((st = device_sms(&sms)) != STREAMKL_OK) return st;
         const int64_t units = int64_t(s->B) * kv_heads(s);
         const int k_tiles = (s->Nk + kBlockK - 1) / kBlockK;
-        pl->splits = choose_splits(units, k_tiles, sms);
+        if (opt && opt->num_splits > 0)
+            pl->splits = opt->num_splits < k_tiles ? opt->num_splits : k_tiles;
+        else
+            pl->splits = choose_splits(units, k_tiles, sms);
         if (units * pl->splits > INT32_MAX) return STREAMKL_ERR_UNSUPPORTED;
         pl->ctas_dec = static_cast<int>(units * pl->splits);
     }

@@ -143,10 +143,10 @@ def fwd_plan(Q1, K1, causal=False, num_splits=0) -> Plan:
     return plan
 
 
-def bwd_plan(Q1, K1, setting, causal=False, mode=BWD_AUTO, grad_dtype=torch.float32) -> Plan:
+def bwd_plan(Q1, K1, setting, causal=False, mode=BWD_AUTO, grad_dtype=torch.float32, num_splits=0) -> Plan:
     plan = Plan()
     _raise(load().streamkl_bwd_plan(ctypes.byref(make_shape(Q1, K1)), int(setting), int(bool(causal)),
-                                    ctypes.byref(_opts(bwd_mode=mode, grad_bf16=_grad_flag(grad_dtype))),
+                                    ctypes.byref(_opts(num_splits, mode, grad_bf16=_grad_flag(grad_dtype))),
                                     ctypes.byref(plan)), "streamkl_bwd_plan")
     return plan
 
@@ -189,14 +189,15 @@ def kl_fwd(Q1, K1, Q2, K2, causal=False, scale=None, num_splits=0, workspace=Non
 
 
 def kl_bwd(setting, g, Q1, K1, Q2, K2, KL, LSE1, LSE2, causal=False, scale=None, mode=BWD_AUTO, workspace=None,
-           out=None, wait_limit_ns=0, debug_flags=0, grad_dtype=torch.float32):
+           out=None, wait_limit_ns=0, debug_flags=0, grad_dtype=torch.float32, num_splits=0):
     """(dQ, dK) float32 of the trainable side: setting 1 -> (Q2, K2), 2 -> (Q1, K1).
     With keys shared by groups of query heads (K has fewer heads than Q), dK
-    has K's head count and sums the gradients of each group."""
+    has K's head count and sums the gradients of each group.  num_splits sets
+    the key-range splits of the key-split mode (0 = automatic)."""
     _check_qk(Q1, K1, Q2, K2)
     lib = load()
     shape = make_shape(Q1, K1)
-    opts = _opts(0, mode, wait_limit_ns, debug_flags, _grad_flag(grad_dtype))
+    opts = _opts(num_splits, mode, wait_limit_ns, debug_flags, _grad_flag(grad_dtype))
     plan = Plan()
     _raise(lib.streamkl_bwd_plan(ctypes.byref(shape), int(setting), int(bool(causal)), ctypes.byref(opts),
                                  ctypes.byref(plan)), "streamkl_bwd_plan")

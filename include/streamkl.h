@@ -82,7 +82,8 @@ typedef struct {
 
 /* Optional knobs; pass NULL for the defaults. */
 typedef struct {
-    int32_t num_splits;    /* forward: 0 = automatic, n >= 1 forces n key splits     */
+    int32_t num_splits;    /* forward and key-split backward: 0 = automatic,        */
+                           /*   n >= 1 forces n key-range splits                    */
     int32_t bwd_mode;      /* backward: 0 = automatic, 1 = fused (atomic dQ),        */
                            /*           2 = separate dQ and dK kernels,               */
                            /*           3 = key-split (needs Nq * H / H_kv <= 16)     */
