@@ -99,20 +99,38 @@ __device__ __forceinline__ void store_ds_chunk(uint32_t tile_hi, uint32_t tile_l
 }
 
 // Store 32 gradient values (scaled) at columns [c0, c0 + 32) of a row, as
-// float32 or as bf16 (round to nearest even).
+// float32 or as bf16 (round to nearest even).  Each thread writes its own
+// row, so a warp's store instruction touches 32 rows: whole 32-byte sectors
+// (when the row is 32-byte aligned) keep those writes sector-sized.
 __device__ __forceinline__ void store_grad32(void* row, int c0, const float (&v)[32], float scale, bool bf16) {
     if (bf16) {
-        uint4* out = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(row) + c0);
+        uint16_t* out = reinterpret_cast<uint16_t*>(row) + c0;
+        uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 8)
-            out[e / 8] = make_uint4(pack_bf16(v[e] * scale, v[e + 1] * scale), pack_bf16(v[e + 2] * scale, v[e + 3] * scale),
-                                    pack_bf16(v[e + 4] * scale, v[e + 5] * scale),
-                                    pack_bf16(v[e + 6] * scale, v[e + 7] * scale));
+        for (int e = 0; e < 16; ++e) w[e] = pack_bf16(v[2 * e] * scale, v[2 * e + 1] * scale);
+        if ((reinterpret_cast<uintptr_t>(out) & 31u) == 0) {
+            st_global_v8(out, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+            st_global_v8(out + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+        } else {
+            uint4* o4 = reinterpret_cast<uint4*>(out);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        }
     } else {
-        float4* out = reinterpret_cast<float4*>(reinterpret_cast<float*>(row) + c0);
+        float* out = reinterpret_cast<float*>(row) + c0;
+        if ((reinterpret_cast<uintptr_t>(out) & 31u) == 0) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-            out[e / 4] = make_float4(v[e] * scale, v[e + 1] * scale, v[e + 2] * scale, v[e + 3] * scale);
+            for (int e = 0; e < 32; e += 8)
+                st_global_v8(out + e, __float_as_uint(v[e] * scale), __float_as_uint(v[e + 1] * scale),
+                             __float_as_uint(v[e + 2] * scale), __float_as_uint(v[e + 3] * scale),
+                             __float_as_uint(v[e + 4] * scale), __float_as_uint(v[e + 5] * scale),
+                             __float_as_uint(v[e + 6] * scale), __float_as_uint(v[e + 7] * scale));
+        } else {
+            float4* o4 = reinterpret_cast<float4*>(out);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+                o4[e / 4] = make_float4(v[e] * scale, v[e + 1] * scale, v[e + 2] * scale, v[e + 3] * scale);
+        }
     }
 }
 

@@ -81,6 +81,8 @@ WORKLOADS = {
     # backward of a decode-shaped problem: 16 query rows against 128K keys, both settings; each
     # 128-key tile is its own CTA, so the key range is split across the whole grid
     "decode_bwd_q16_k128k": Workload("decode_bwd_q16_k128k", 4, 32, 16, 131072, 128, 0.3, False, seed=8),
+    # one batch of it, small enough for a full ncu capture (2 GiB of keys)
+    "decode_bwd_q16_k128k_b1": Workload("decode_bwd_q16_k128k_b1", 1, 32, 16, 131072, 128, 0.3, False, seed=8),
     # one batch of the 128K decode: small enough for a full ncu capture (2 GiB of keys)
     "decode_q1_k128k_b1": Workload("decode_q1_k128k_b1", 1, 32, 1, 131072, 128, 0.3, False, seed=3,
                                    fwd_only=True),

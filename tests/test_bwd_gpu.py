@@ -182,3 +182,29 @@ def test_bf16_gradient_outputs(setting, mode):
         torch.testing.assert_close(dQ.float(), f32[0].to(torch.bfloat16).float(), rtol=2.0 ** -7, atol=1e-30)
     else:
         torch.testing.assert_close(dQ, f32[0].to(torch.bfloat16), rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("mode", [FUSED, SPLIT, streamkl.BWD_KEYSPLIT])
+def test_outputs_aligned_to_16_bytes_only(mode):
+    """Gradient buffers that start 16 bytes past a 32-byte boundary (the ABI
+    asks for 16): rows are written with 16-byte stores there."""
+    Nq = 8 if mode == streamkl.BWD_KEYSPLIT else 200
+    Q1, K1, Q2, K2 = make_qk(1, 2, Nq, 700, 128, 0.4, seed=31, device=DEV)
+    g = torch.rand((1, 2, Nq), device=DEV) + 0.5
+    KL, L1, L2 = streamkl.kl_fwd(Q1, K1, Q2, K2)
+
+    def offset_empty(shape):
+        n = int(np.prod(shape))
+        buf = torch.empty(n + 4, dtype=torch.float32, device=DEV)
+        view = buf[4:].view(shape)
+        assert view.data_ptr() % 32 == 16
+        return view
+
+    out = (offset_empty(Q1.shape), offset_empty(K1.shape))
+    dQ, dK = streamkl.kl_bwd(1, g, Q1, K1, Q2, K2, KL, L1, L2, mode=mode, out=out)
+    ref = streamkl.kl_bwd(1, g, Q1, K1, Q2, K2, KL, L1, L2, mode=mode)
+    torch.cuda.synchronize()
+    rdQ, rdK = oracle.bwd(1, g, Q1, K1, Q2, K2, causal=False)
+    assert_grad(dQ, rdQ, "dQ (16-byte aligned output)")
+    assert_grad(dK, rdK, "dK (16-byte aligned output)")
+    torch.testing.assert_close(dK, ref[1], rtol=0, atol=0)
