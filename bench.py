@@ -50,6 +50,8 @@ TRAFFIC = {
     ("64k_causal", "fwd"): 2.17e9 + 0.038e9,
     ("64k_causal", "bwd_setting1"): 3.31e9 + 2.21e9,
     ("64k_causal", "bwd_setting2"): 3.33e9 + 2.21e9,
+    ("decode_bwd_q16_k128k", "bwd_setting1"): 8.81e9 + 8.54e9,
+    ("decode_bwd_q16_k128k", "bwd_setting2"): 8.80e9 + 8.54e9,
 }
 
 
