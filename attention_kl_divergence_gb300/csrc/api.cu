@@ -50,6 +50,7 @@ streamkl_status device_sms(int* sms) {
 // on `slots` resident CTAs: minimise waves * (tiles per split + 1 tile of
 // fixed cost), preferring fewer splits on ties.
 int choose_splits(int64_t units, int k_tiles, int slots) {
+    // (used by the tile forward and the key-split backward; decode_splits below for the decode forward)
     if (units >= slots || k_tiles < 2) return 1;
     int best = 1;
     int64_t best_cost = INT64_MAX;
@@ -63,6 +64,20 @@ int choose_splits(int64_t units, int k_tiles, int slots) {
         }
     }
     return best;
+}
+
+// Key splits of the decode forward, which streams every key byte once and is
+// bound by HBM: measured on GB300, about 0.7 x SMs streaming CTAs saturate it
+// (32 CTAs 2.7 TB/s, 64 5.2, 96-128 6.1), so the key range is split only until
+// that many CTAs exist.  More splits add partial states and a second wave
+// (B4 H32, 16 rows: 1 split 1.25 ms, 13 splits 1.32 ms).
+int decode_splits(int64_t units, int k_tiles, int sms) {
+    const int64_t saturate = (int64_t(sms) * 7 + 9) / 10;
+    if (units >= saturate) return 1;
+    int64_t s = (saturate + units - 1) / units;
+    if (s > k_tiles) s = k_tiles;
+    if (s > kMaxSplits) s = kMaxSplits;
+    return s < 1 ? 1 : static_cast<int>(s);
 }
 
 struct FwdPlan {
@@ -101,6 +116,8 @@ streamkl_status plan_fwd(const streamkl_shape* s, int causal, const streamkl_opt
     int splits;
     if (opt && opt->num_splits > 0)
         splits = opt->num_splits < pl->num_k_tiles ? opt->num_splits : pl->num_k_tiles;
+    else if (pl->decode)
+        splits = decode_splits(units, pl->num_k_tiles, sms);
     else
         splits = choose_splits(units, pl->num_k_tiles, sms);
     if (splits > kMaxSplits) splits = kMaxSplits;

@@ -414,6 +414,67 @@ def run_reference(args):
     }
 
 
+def run_ablations(args):
+    """Design ablations, one JSON line each (not the benchmark contract line):
+    the decode forward with its key range unsplit vs the automatic split, and
+    the backward modes (fused, separate kernels, key-split) on the shapes each
+    is meant for.  Medians of CUDA-event timings with L2 flushed before each."""
+    from attention_kl_divergence_gb300 import streamkl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    l2_flush = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn, reps):
+        for _ in range(args.warmup):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush_l2(l2_flush)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    def emit(**kw):
+        print(json.dumps(dict(ablation=True, **kw)), flush=True)
+
+    # Split-K on the decode workloads: one CTA per head (splits = 1) vs the automatic choice
+    for name in ("decode_q1_k128k", "decode_q16_k128k", "decode_q1_k512k", "decode_q16_k512k"):
+        w = WORKLOADS[name]
+        Q1, K1, Q2, K2 = make_workload(w, device=dev)
+        out = tuple(torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev) for _ in range(3))
+        for splits in (1, 0):
+            plan = streamkl.fwd_plan(Q1, K1, num_splits=splits)
+            ms = timed(lambda: streamkl.kl_fwd(Q1, K1, Q2, K2, num_splits=splits, out=out), max(args.steps, 5))
+            emit(what="decode split-K", workload=name, splits=plan.num_splits, ms=ms,
+                 gbs=w.fwd_bytes() / ms / 1e6)
+        del Q1, K1, Q2, K2
+        torch.cuda.empty_cache()
+    # backward modes
+    modes = {"fused": streamkl.BWD_FUSED, "split": streamkl.BWD_SPLIT, "keysplit": streamkl.BWD_KEYSPLIT}
+    for name, names in (("8k_causal", ("fused", "split")), ("64k_causal", ("fused", "split")),
+                        ("decode_bwd_q16_k128k", ("keysplit", "fused", "split"))):
+        w = WORKLOADS[name]
+        Q1, K1, Q2, K2 = make_workload(w, device=dev)
+        g = make_g(w.B, w.H, w.Nq, w.g_value, device=dev)
+        KL, L1, L2 = streamkl.kl_fwd(Q1, K1, Q2, K2, causal=w.causal)
+        grads = (torch.empty_like(Q1, dtype=torch.float32), torch.empty_like(K1, dtype=torch.float32))
+        reps = 3 if w.Nq >= 65536 else max(args.steps, 5)
+        for setting in (1, 2):
+            for mname in names:
+                ms = timed(lambda: streamkl.kl_bwd(setting, g, Q1, K1, Q2, K2, KL, L1, L2, causal=w.causal,
+                                                   mode=modes[mname], out=grads), reps)
+                emit(what="backward mode", workload=name, setting=setting, mode=mname, ms=ms,
+                     tflops=8 * w.d * w.visible_pairs() * w.B * w.H / ms / 1e9, gbs=w.bwd_bytes() / ms / 1e6)
+        del Q1, K1, Q2, K2, grads
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -423,7 +484,12 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(WORKLOADS),
                     help="another named workload (the headline metric is quoted on 64k_causal)")
+    ap.add_argument("--ablate", action="store_true",
+                    help="print the design ablations (split-K, backward modes) instead of the benchmark line")
     args = ap.parse_args()
+    if args.ablate:
+        run_ablations(args)
+        return
     if args.warmup < 3 and args.impl != "reference":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":

@@ -101,17 +101,23 @@ def test_64k_noncausal_forward_and_both_settings():
         assert cos > 0.99999 and rel < 1e-2, (cos, rel)
 
 
+@pytest.mark.parametrize("splits", [0, 13])
 @pytest.mark.parametrize("name", ["decode_q1_k128k", "decode_q16_k128k", "decode_q1_k512k", "decode_q16_k512k",
-                                  "decode_causal_q16_k128k", "decode_gqa_q1_k128k"])
-def test_decode_split_k_all_rows_of_sampled_heads(name):
+                                  "decode_causal_q16_k128k", "decode_gqa_q1_k128k", "decode_q1_k128k_b1"])
+def test_decode_split_k_all_rows_of_sampled_heads(name, splits):
+    """Automatic splits (one CTA per head once there are enough heads to keep
+    HBM busy) and 13 forced splits with the combine step."""
     w = WORKLOADS[name]
     inputs = make_workload(w, device=DEV)
-    plan = streamkl.fwd_plan(inputs[0], inputs[1], causal=w.causal)
-    assert plan.path == streamkl.PATH_DECODE and plan.num_splits > 1
-    KL, L1, L2 = streamkl.kl_fwd(*inputs, causal=w.causal)
+    plan = streamkl.fwd_plan(inputs[0], inputs[1], causal=w.causal, num_splits=splits)
+    assert plan.path == streamkl.PATH_DECODE
+    if splits:
+        assert plan.num_splits == splits and plan.launches == 2
+    KL, L1, L2 = streamkl.kl_fwd(*inputs, causal=w.causal, num_splits=splits)
     torch.cuda.synchronize()
     group = w.H // (w.H_kv or w.H)
-    for bh in (0, 37, 64, w.B * w.H - 1):
+    nbh = w.B * w.H
+    for bh in sorted({0, 37 % nbh, 64 % nbh, nbh - 1}):
         b, h = divmod(bh, w.H)
         q1, k1, q2, k2 = inputs
         hq = [head(q1, bh), k1[b, h // group][None, None], head(q2, bh), k2[b, h // group][None, None]]
