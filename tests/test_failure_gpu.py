@@ -31,18 +31,22 @@ def test_forward_wait_timeout_is_reported(Nq, Nk, causal):
     assert_kl(KL, rKL)
 
 
-@pytest.mark.parametrize("mode", [streamkl.BWD_FUSED, streamkl.BWD_SPLIT])
-def test_backward_wait_timeout_is_reported(mode):
-    Q1, K1, Q2, K2 = make_qk(1, 2, 600, 600, 128, 0.3, seed=11, device=DEV)
-    g = make_g(1, 2, 600, 1.0, device=DEV)
-    KL, L1, L2 = streamkl.kl_fwd(Q1, K1, Q2, K2, causal=True)
+@pytest.mark.parametrize("mode,Nq,Nk,causal", [
+    (streamkl.BWD_FUSED, 600, 600, True),
+    (streamkl.BWD_SPLIT, 600, 600, True),
+    (streamkl.BWD_KEYSPLIT, 8, 5000, False),
+])
+def test_backward_wait_timeout_is_reported(mode, Nq, Nk, causal):
+    Q1, K1, Q2, K2 = make_qk(1, 2, Nq, Nk, 128, 0.3, seed=11, device=DEV)
+    g = make_g(1, 2, Nq, 1.0, device=DEV)
+    KL, L1, L2 = streamkl.kl_fwd(Q1, K1, Q2, K2, causal=causal)
     ws = streamkl.new_workspace(256, DEV)
-    streamkl.kl_bwd(1, g, Q1, K1, Q2, K2, KL, L1, L2, causal=True, mode=mode, workspace=ws, **STALL)
+    streamkl.kl_bwd(1, g, Q1, K1, Q2, K2, KL, L1, L2, causal=causal, mode=mode, workspace=ws, **STALL)
     torch.cuda.synchronize()
     assert streamkl.workspace_status(ws) != 0
-    dQ, dK = streamkl.kl_bwd(1, g, Q1, K1, Q2, K2, KL, L1, L2, causal=True, mode=mode, workspace=ws)
+    dQ, dK = streamkl.kl_bwd(1, g, Q1, K1, Q2, K2, KL, L1, L2, causal=causal, mode=mode, workspace=ws)
     torch.cuda.synchronize()
     assert streamkl.workspace_status(ws) == 0
-    rdQ, rdK = oracle.bwd(1, g, Q1, K1, Q2, K2, causal=True)
+    rdQ, rdK = oracle.bwd(1, g, Q1, K1, Q2, K2, causal=causal)
     assert_grad(dQ, rdQ, "dQ after a timed-out call")
     assert_grad(dK, rdK, "dK after a timed-out call")
