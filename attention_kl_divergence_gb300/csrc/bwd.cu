@@ -147,22 +147,28 @@ __global__ void __launch_bounds__(320, 1)
             const uint32_t t_dq = tmem + 256;
             int issued = 0;
             bool started = false;
-            auto issue_s = [&](int it) {
-                const int s = it % NST, buf = it & 1;
-                const uint32_t k1s = base + L::k + 2 * s * L::kKBytes;
+            // few instructions per MMA: descriptor low words advance by compile-time
+            // offsets (the high word is one constant); ring positions are counters
+            const uint32_t dhi = smem_desc_hi();
+            constexpr uint32_t kStageLo = (2 * L::kKBytes) >> 4, kK2Lo = L::kKBytes >> 4;
+            const uint32_t q1_lo = smem_desc_lo_k128(base + L::q1), q2_lo = smem_desc_lo_k128(base + L::q2);
+            const uint32_t k_lo0 = smem_desc_lo_k128(base + L::k);
+            const uint32_t kt_lo0 = smem_desc_lo_mn128(base + L::k + kt_off, kBwdTile * 128);
+            const uint32_t ds_lo = smem_desc_lo_k128(base + L::ds);
+            static_assert(L::kNumDs == 1, "one dS buffer");
+            auto issue_s = [&](int buf, uint32_t k_lo) {
                 const uint32_t d1 = tmem + buf * 128, d2 = d1 + 64;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t qo = (kk >> 2) * kBlockQ * 128 + (kk & 3) * 32;
-                    const uint32_t ko = (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32;
-                    tc_mma_bf16(d1, smem_desc_k128(base + L::q1 + qo), smem_desc_k128(k1s + ko), id_s, kk > 0);
+                    const uint32_t qo = ((kk >> 2) * kBlockQ * 128 + (kk & 3) * 32) >> 4;
+                    const uint32_t ko = ((kk >> 2) * kBwdTile * 128 + (kk & 3) * 32) >> 4;
+                    tc_mma_bf16_w(d1, q1_lo + qo, dhi, k_lo + ko, dhi, id_s, kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t qo = (kk >> 2) * kBlockQ * 128 + (kk & 3) * 32;
-                    const uint32_t ko = (kk >> 2) * kBwdTile * 128 + (kk & 3) * 32;
-                    tc_mma_bf16(d2, smem_desc_k128(base + L::q2 + qo), smem_desc_k128(k1s + L::kKBytes + ko), id_s,
-                                kk > 0);
+                    const uint32_t qo = ((kk >> 2) * kBlockQ * 128 + (kk & 3) * 32) >> 4;
+                    const uint32_t ko = ((kk >> 2) * kBwdTile * 128 + (kk & 3) * 32) >> 4;
+                    tc_mma_bf16_w(d2, q2_lo + qo, dhi, k_lo + kK2Lo + ko, dhi, id_s, kk > 0);
                 }
                 tc_commit(base + L::bar_sfull + 8 * buf);
             };
@@ -173,32 +179,32 @@ __global__ void __launch_bounds__(320, 1)
                       mbar_wait(base + L::bar_kfull, 0, wc, kErrWaitK);
             if (ok) {
                 tc_fence_after();
-                issue_s(0);
+                issue_s(0, k_lo0);
                 started = true;
+                int sn = NST > 1 ? 1 : 0, s = 0;    // stages of tiles it + 1 and it
+                uint32_t pn = NST > 1 ? 0 : 1;      // phase of tile it + 1's stage
                 for (int it = 0; it < n_tiles; ++it) {
                     if (it + 1 < n_tiles) {
                         const int n1 = it + 1;
-                        if (!mbar_wait(base + L::bar_kfull + 8 * (n1 % NST), (n1 / NST) & 1, wc, kErrWaitK)) break;
+                        if (!mbar_wait(base + L::bar_kfull + 8 * sn, pn, wc, kErrWaitK)) break;
                         if (!mbar_wait(base + L::bar_sempty + 8 * (n1 & 1), ((n1 >> 1) & 1) ^ 1, wc, kErrWaitS))
                             break;
                         tc_fence_after();
-                        issue_s(n1);
+                        issue_s(n1 & 1, k_lo0 + sn * kStageLo);
+                        if (++sn == NST) sn = 0, pn ^= 1;
                     }
-                    const int s = it % NST;
-                    const int dsb = it % L::kNumDs;
-                    if (!mbar_wait(base + L::bar_dsfull + 8 * dsb, (it / L::kNumDs) & 1, wc, kErrWaitOther)) break;
+                    if (!mbar_wait(base + L::bar_dsfull, it & 1, wc, kErrWaitOther)) break;
                     tc_fence_after();
-                    const uint32_t kts = base + L::k + 2 * s * L::kKBytes + kt_off;
-                    const uint32_t dss = base + L::ds + 2 * dsb * L::kDsBytes;
+                    const uint32_t kt_lo = kt_lo0 + s * kStageLo;
 #pragma unroll
                     for (int part = 0; part < 2; ++part)  // dS = hi + lo
 #pragma unroll
                         for (int kk = 0; kk < kBwdTile / 16; ++kk)
-                            tc_mma_bf16(t_dq, smem_desc_k128(dss + part * L::kDsBytes + kk * 32),
-                                        smem_desc_mn128(kts + kk * 16 * 128, kBwdTile * 128), id_dq,
-                                        (it | kk | part) != 0);
-                    tc_commit(base + L::bar_dsempty + 8 * dsb);
+                            tc_mma_bf16_w(t_dq, ds_lo + ((part * L::kDsBytes + kk * 32) >> 4), dhi,
+                                          kt_lo + ((kk * 16 * 128) >> 4), dhi, id_dq, (it | kk | part) != 0);
+                    tc_commit(base + L::bar_dsempty);
                     tc_commit(base + L::bar_kempty + 8 * s);
+                    if (++s == NST) s = 0;
                     ++issued;
                 }
                 if (issued == n_tiles) tc_commit(base + L::bar_done);
@@ -219,6 +225,9 @@ __global__ void __launch_bounds__(320, 1)
         const size_t grow = static_cast<size_t>(bh) * p.Nq + i;
         float la, xb, g;
         row_constants<SETTING>(p, grow, i < p.Nq, la, xb, g);
+        // the row's constants as FP32x2 pairs; the softmax scale of dQ is folded into g
+        const float2 cc = make_float2(c, c), sc2 = make_float2(p.scale, p.scale), nla = make_float2(-la, -la),
+                     nxb = make_float2(-xb, -xb), gs = make_float2(g * p.scale, g * p.scale);
         const int limit = p.causal ? min(i + p.diag_off, p.Nk - 1) : p.Nk - 1;
         bool ok = true;
         for (int it = 0; it < n_tiles; ++it) {
@@ -239,15 +248,17 @@ __global__ void __launch_bounds__(320, 1)
             mbar_arrive(base + L::bar_sempty + 8 * buf);
             const int last = limit - (it * kBwdTile + wg * 32);
             float v[32];
-            if (last >= 31) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = dscore<SETTING>(z1[e], z2[e], c, p.scale, la, xb, g);
-            } else {
+            for (int e = 0; e < 32; e += 2) {
+                const float2 d = dscore2<SETTING>(make_float2(z1[e], z1[e + 1]), make_float2(z2[e], z2[e + 1]), cc,
+                                                  sc2, nla, nxb, gs);
+                v[e] = d.x;
+                v[e + 1] = d.y;
+            }
+            if (last < 31) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    v[e] = dscore<SETTING>(z1[e], z2[e], c, p.scale, la, xb, g);
+                for (int e = 0; e < 32; ++e)
                     if (e > last) v[e] = 0.f;
-                }
             }
             if (!wait_all(base + L::bar_dsempty + 8 * dsb, ((it / L::kNumDs) & 1) ^ 1, wc, kErrWaitOther)) {
                 ok = false;
@@ -266,7 +277,7 @@ __global__ void __launch_bounds__(320, 1)
                 float v[32];
                 tmem_ld32(tl + 256 + c0, v);
                 tc_wait_ld();
-                if (i < p.Nq) store_grad32(out, c0, v, p.scale, p.grad_bf16 != 0);
+                if (i < p.Nq) store_grad32(out, c0, v, 1.0f, p.grad_bf16 != 0);  // the scale is in dS
             }
         }
     }
