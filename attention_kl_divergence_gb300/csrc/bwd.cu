@@ -719,13 +719,15 @@ __global__ void __launch_bounds__(kv_threads<FUSED>(), 1)
         // ------------------------------------------------ dQ^T -> bulk L2 reduction into dQ
         // Each tile's 64 x d float32 block of dQ is staged in shared memory as
         // 64 contiguous rows (the non-trainable key tile's space: that tile
-        // only fed the copy into tensor memory) and added to global dQ with
-        // one bulk reduce-add.
+        // only fed the copy into tensor memory) and added to global dQ by bulk
+        // reduce-adds, one per 32-row half, so that staging one half overlaps
+        // the reduction still reading the other.
         const int wq = warp & 3;
         const int f = wq * 32 + lane;  // feature = TMEM lane
         const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
         const uint32_t stage = base + (SETTING == 1 ? L::k1 : L::k2);
         const bool leader = warp == 10 && lane == 0;
+        bool other_pending = false;  // the last bulk group issued was the other half's
         for (int m = 0; m < n_tiles; ++m) {
             // the four epilogue warps decide together, so none is left at a named barrier
             if (!bar_sync_and(3, 128, wait_all(base + L::bar_dqfull, m & 1, wc, kErrWaitOther))) break;
@@ -754,24 +756,35 @@ __global__ void __launch_bounds__(kv_threads<FUSED>(), 1)
             }
             tc_fence_before();
             mbar_arrive(base + L::bar_dqempty);
-            if (leader) bulk_wait_read_all();  // the previous tile's reduction has read the stage
-            asm volatile("bar.sync 2, 128;" ::: "memory");
-            if (f < D) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(stage + e * (D * 4) + f * 4), "f"(v0[e]) : "memory");
-                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(stage + (e + 32) * (D * 4) + f * 4), "f"(v1[e])
-                                 : "memory");
-                }
-            }
-            fence_proxy_async_smem();
-            asm volatile("bar.sync 2, 128;" ::: "memory");
             const int r0 = qtile(m) * kBwdTile;
             const int nrow = min(kBwdTile, p.Nq - r0);
-            if (leader && nrow > 0) {
-                bulk_reduce_add_f32(p.dQacc + ((static_cast<size_t>(b) * p.H + qhead(m)) * p.Nq + r0) * D, stage,
-                                    static_cast<uint32_t>(nrow * D * 4));
-                bulk_commit();
+            float* dst = p.dQacc + ((static_cast<size_t>(b) * p.H + qhead(m)) * p.Nq + r0) * D;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const uint32_t sh = stage + hf * 32 * (D * 4);
+                // the reduction that last read this half has finished reading; when the
+                // other half's reduction was the last one issued it may still run
+                if (leader) {
+                    if (other_pending)
+                        bulk_wait_read_1();
+                    else
+                        bulk_wait_read_all();
+                }
+                asm volatile("bar.sync 2, 128;" ::: "memory");
+                if (f < D) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        asm volatile("st.shared.f32 [%0], %1;" ::"r"(sh + e * (D * 4) + f * 4), "f"(hf ? v1[e] : v0[e])
+                                     : "memory");
+                }
+                fence_proxy_async_smem();
+                asm volatile("bar.sync 2, 128;" ::: "memory");
+                const int rows = min(32, nrow - 32 * hf);
+                other_pending = rows > 0;
+                if (leader && rows > 0) {
+                    bulk_reduce_add_f32(dst + hf * 32 * D, sh, static_cast<uint32_t>(rows * D * 4));
+                    bulk_commit();
+                }
             }
         }
         if (leader) bulk_wait_all();  // every reduction has landed before the CTA exits

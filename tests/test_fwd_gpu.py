@@ -106,6 +106,18 @@ def test_large_scores_do_not_overflow():
     run_and_check(Q1 * 3, K1, Q2 * 3, K2, False)
 
 
+@pytest.mark.parametrize("causal,splits", [(False, 1), (True, 1), (False, 3)])
+def test_scores_rising_along_the_keys(causal, splits):
+    """Key norms grow with the key index, so a row's maximum keeps rising far
+    above the reference the update holds: unmasked pieces well after a row's
+    first must raise it again (and pieces that stay below it must be kept)."""
+    Q1, K1, Q2, K2 = make_qk(1, 2, 520, 1500, 128, 0.3, teacher_scale=1.5, seed=21, device=DEV)
+    ramp = torch.linspace(0.2, 6.0, 1500, device=DEV).view(1, 1, -1, 1)
+    K1 = (K1.float() * ramp).to(torch.bfloat16)
+    K2 = (K2.float() * ramp).to(torch.bfloat16)
+    run_and_check(Q1, K1, Q2, K2, causal, splits)
+
+
 def test_plan_uses_splits_when_the_grid_is_small():
     Q1, K1, _, _ = make_qk(1, 1, 256, 32768, 128, 0.3, seed=1, device=DEV)
     assert streamkl.fwd_plan(Q1, K1).num_splits > 1
