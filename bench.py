@@ -48,8 +48,8 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # version they were taken on: reset to None whenever that kernel changes.
 TRAFFIC = {
     ("64k_causal", "fwd"): 2.17e9 + 0.038e9,
-    ("64k_causal", "bwd_setting1"): 3.31e9 + 2.21e9,
-    ("64k_causal", "bwd_setting2"): 3.33e9 + 2.21e9,
+    ("64k_causal", "bwd_setting1"): 3.350e9 + 2.250e9,
+    ("64k_causal", "bwd_setting2"): 3.364e9 + 2.252e9,
     ("decode_bwd_q16_k128k", "bwd_setting1"): 8.81e9 + 8.54e9,
     ("decode_bwd_q16_k128k", "bwd_setting2"): 8.80e9 + 8.54e9,
 }
@@ -268,13 +268,16 @@ def run_gpu(args):
     step_flops = f_fwd + (2 * f_bwd if with_bwd else 0)
     value = step_flops * ws_ / (step_ms * 1e-3) / 1e12
     peak_tf = peaks["bf16_tflops"]
+    peak_sus = peaks.get("bf16_tflops_sustained", PEAKS_FALLBACK["bf16_tflops_sustained"])
     kernels = {"fwd": {"ms": fwd_ms, "tflops": f_fwd / fwd_ms / 1e9, "frac_bf16_peak": f_fwd / fwd_ms / 1e9 / peak_tf,
+                       "frac_bf16_sustained": f_fwd / fwd_ms / 1e9 / peak_sus,
                        "gbs": w.fwd_bytes() / fwd_ms / 1e6, "frac_hbm_peak": w.fwd_bytes() / fwd_ms / 1e6 /
                        peaks["hbm_gbs"], "path": "tile" if fplan.path == 0 else "decode",
                        "splits": fplan.num_splits}}
     if with_bwd:
         for name, ms, plan in (("bwd_setting1", b1_ms, bplan1), ("bwd_setting2", b2_ms, bplan2)):
             kernels[name] = {"ms": ms, "tflops": f_bwd / ms / 1e9, "frac_bf16_peak": f_bwd / ms / 1e9 / peak_tf,
+                             "frac_bf16_sustained": f_bwd / ms / 1e9 / peak_sus,
                              "gbs": w.bwd_bytes() / ms / 1e6, "frac_hbm_peak": w.bwd_bytes() / ms / 1e6 /
                              peaks["hbm_gbs"],
                              "mode": BWD_MODE_NAMES[plan.path]}
@@ -308,10 +311,17 @@ def run_gpu(args):
     else:
         flops_top = f_fwd if top == "fwd" else f_bwd
         achieved = flops_top / kernels[top]["ms"] / 1e9
-        roofline = {"kernel": names[top], "bound": "tensor", "achieved": achieved, "peak": peak_tf,
-                    "unit": "TFLOP/s", "frac": achieved / peak_tf, "traffic": traffic_for(w.name, top),
+        # The kernel is timed inside the step: in a long step (tens of ms and more of
+        # back-to-back tensor work) the GPU sits at its power cap, where the measured
+        # sustained GEMM rate is the ceiling; a short step runs at the burst rate.
+        long_step = step_ms >= 50.0
+        peak = peak_sus if long_step else peak_tf
+        roofline = {"kernel": names[top], "bound": "tensor", "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak, "frac_of_burst_peak": achieved / peak_tf,
+                    "traffic": traffic_for(w.name, top),
                     "share_of_step": kernels[top]["ms"] / step_ms, "flops_per_launch": flops_top,
-                    "peak_source": f"bf16_tflops ({peak_src}, burst)"}
+                    "peak_source": (f"bf16_tflops_sustained ({peak_src}; timed inside a {step_ms:.0f} ms step)"
+                                    if long_step else f"bf16_tflops ({peak_src}, burst)")}
 
     # ---------------- end to end through the C ABI with host buffers
     pin = dict(pin_memory=True)
