@@ -90,6 +90,25 @@ def test_64k_causal_forward_and_both_settings():
     run_workload("64k_causal", (1, 2), heads=(0, 13, 31), key_tail=1024)
 
 
+def test_64k_causal_dk_of_keys_across_the_sequence():
+    """dK of keys spread over one whole 64K causal head, the first keys
+    included: their gradient sums over every query row of the sequence, the
+    longest accumulation the fused kernel keeps in tensor memory.  The oracle
+    computes the statistics of all 65536 rows of the head once (~1e12 flops)."""
+    w = WORKLOADS["64k_causal"]
+    inputs = make_workload(w, device=DEV)
+    KL, L1, L2 = streamkl.kl_fwd(*inputs, causal=w.causal)
+    g = make_g(w.B, w.H, w.Nq, w.g_value, device=DEV)
+    dQ, dK = streamkl.kl_bwd(1, g, *inputs, KL, L1, L2, causal=w.causal)
+    torch.cuda.synchronize()
+    bh = 13
+    keys = np.array([0, 1, 127, 128, 129, 4095, 16384, 32767, 32768, 49151, w.Nk - 129, w.Nk - 1], dtype=np.int64)
+    rk = oracle.bwd_dk_keys(1, g.reshape(-1, w.Nq)[bh][None, None], *[head(t, bh) for t in inputs], keys,
+                            causal=w.causal)
+    gk = dK.reshape(-1, w.Nk, w.d)[bh][torch.as_tensor(keys, device=DEV)]
+    assert_grad(gk, rk, "dK of keys across a 64K causal head (setting 1)")
+
+
 def test_64k_noncausal_forward_and_both_settings():
     inputs, KL, L1, L2, g = run_workload("64k", (1, 2), heads=(0, 31), rows_per_head=24)
     # fused and split backward agree at full size (the split recomputes independently)
