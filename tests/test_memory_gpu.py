@@ -21,7 +21,7 @@ def peak_extra(fn):
     return torch.cuda.max_memory_allocated() - base, out
 
 
-@pytest.mark.parametrize("N", [4096, 16384, 65536])
+@pytest.mark.parametrize("N", [4096, 16384, 65536, 524288])
 def test_extra_memory_is_linear(N):
     B, H, d = 1, 4, 128
     Q1, K1, Q2, K2 = make_qk(B, H, N, N, d, 0.3, seed=1, device=DEV)
