@@ -78,10 +78,13 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+    _count = 0
+
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join("/tmp", f"streamkl_clocks_{os.getpid()}.csv")
+        ClockSampler._count += 1  # one file per sampler: several may run in one process
+        self.path = os.path.join("/tmp", f"streamkl_clocks_{os.getpid()}_{ClockSampler._count}.csv")
 
     def __enter__(self):
         try:
@@ -256,6 +259,7 @@ def run_gpu(args):
             e[3].record(stream)
         torch.cuda.synchronize()
     barrier(ws_)
+    step_clocks = clk.summary()
     status = streamkl.workspace_status(wsp)
     fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
     b1_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
@@ -375,13 +379,14 @@ def run_gpu(args):
     torch.cuda.synchronize()
     barrier(ws_)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    run_e2e(args.steps, start=a)
-    b.record(stream)
-    torch.cuda.synchronize()
+    with ClockSampler(gpu_id(dev)) as e2e_clk:
+        a.record(stream)
+        run_e2e(args.steps, start=a)
+        b.record(stream)
+        torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, ws_, dev)
     e2e = {"value": step_flops * ws_ / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "clocks": e2e_clk.summary()}
     kl_mean = float(hKL.double().mean())
 
     out = None
@@ -395,7 +400,7 @@ def run_gpu(args):
             "device_error_word": status, "kl_mean": kl_mean,
             "peaks": {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"], "source": peak_src},
         }
-        out["clocks"] = clk.summary()
+        out["clocks"] = step_clocks
     return out, w
 
 
