@@ -6,7 +6,7 @@ import torch
 
 from attention_kl_divergence_gb300 import WORKLOADS, make_g, make_qk, make_workload, streamkl
 from oracle import oracle
-from parity import assert_grad, grad_report
+from parity import assert_grad, assert_kl, assert_lse, grad_report
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -208,3 +208,46 @@ def test_outputs_aligned_to_16_bytes_only(mode):
     assert_grad(dQ, rdQ, "dQ (16-byte aligned output)")
     assert_grad(dK, rdK, "dK (16-byte aligned output)")
     torch.testing.assert_close(dK, ref[1], rtol=0, atol=0)
+
+
+MODES = {"fused": FUSED, "split": SPLIT, "keysplit": streamkl.BWD_KEYSPLIT}
+
+
+@pytest.mark.parametrize("mode", sorted(MODES))
+@pytest.mark.parametrize("setting", [1, 2])
+def test_signed_and_zero_upstream_gradient(setting, mode):
+    """g is any real per-row weight: mixed signs and exact zeros (rows that
+    contribute nothing) in every backward path."""
+    Nq, Nk, causal = (16, 900, False) if mode == "keysplit" else (200, 333, True)
+    Q1, K1, Q2, K2 = make_qk(1, 2, Nq, Nk, 128, 0.4, seed=5 * Nq + setting, device=DEV)
+    gen = torch.Generator(device="cpu").manual_seed(17 + setting)
+    g = torch.randn((1, 2, Nq), generator=gen)
+    g[:, :, ::5] = 0.0
+    g = g.to(DEV)
+    assert streamkl.bwd_plan(Q1, K1, setting, causal, MODES[mode]).path == {
+        "fused": streamkl.PATH_BWD_FUSED, "split": streamkl.PATH_BWD_SPLIT,
+        "keysplit": streamkl.PATH_BWD_KEYSPLIT}[mode]
+    check_full(setting, Q1, K1, Q2, K2, g, causal, MODES[mode])
+
+
+@pytest.mark.parametrize("mode", sorted(MODES))
+@pytest.mark.parametrize("scale", [0.05, 0.3])
+def test_softmax_scale_other_than_the_default(scale, mode):
+    """An explicit softmax scale (not d^-1/2) reaches the forward and both
+    gradients, which carry it through S = scale Q K^T."""
+    Nq, Nk, causal = (16, 700, False) if mode == "keysplit" else (150, 300, True)
+    Q1, K1, Q2, K2 = make_qk(1, 2, Nq, Nk, 64, 0.5, seed=int(scale * 100) + Nq, device=DEV)
+    KL, L1, L2 = streamkl.kl_fwd(Q1, K1, Q2, K2, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    rKL, rL1, rL2 = oracle.fwd(Q1, K1, Q2, K2, causal=causal, scale=scale)
+    assert_lse(L1, rL1, "LSE1")
+    assert_lse(L2, rL2, "LSE2")
+    assert_kl(KL, rKL)
+    g = torch.rand((1, 2, Nq), device=DEV) + 0.5
+    for setting in (1, 2):
+        dQ, dK = streamkl.kl_bwd(setting, g, Q1, K1, Q2, K2, KL, L1, L2, causal=causal, scale=scale,
+                                 mode=MODES[mode])
+        torch.cuda.synchronize()
+        rdQ, rdK = oracle.bwd(setting, g, Q1, K1, Q2, K2, causal=causal, scale=scale)
+        assert_grad(dQ, rdQ, f"dQ (setting {setting}, scale {scale})")
+        assert_grad(dK, rdK, f"dK (setting {setting}, scale {scale})")
