@@ -45,6 +45,7 @@ def test_tiny_workload(setting):
     (1, 2, 257, 1000, True),
     (1, 1, 1, 700, False),
     (1, 1, 64, 64, False),
+    (1, 2, 700, 130, False),  # more query rows than keys
 ])
 def test_shapes_d128(B, H, Nq, Nk, causal, setting, mode):
     Q1, K1, Q2, K2 = make_qk(B, H, Nq, Nk, 128, 0.4, seed=Nq * 3 + Nk, device=DEV)

@@ -41,6 +41,8 @@ def test_tiny_workload_full():
     (1, 1, 300, 5000, 64, True, 0),
     (2, 1, 513, 700, 128, False, 5),
     (1, 4, 384, 384, 128, True, 1),
+    (1, 2, 700, 130, 128, False, 0),  # more query rows than keys
+    (1, 1, 300, 1, 64, False, 0),     # a single key: KL = 0, LSE = the one score
 ])
 def test_tile_forward_shapes(B, H, Nq, Nk, d, causal, splits):
     Q1, K1, Q2, K2 = make_qk(B, H, Nq, Nk, d, 0.5, seed=Nq + Nk, device=DEV)
