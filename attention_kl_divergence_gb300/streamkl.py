@@ -130,6 +130,31 @@ def _check_qk(Q1, K1, Q2, K2):
         raise ValueError("Q and K must share B and d")
     if Q1.shape[1] % K1.shape[1] != 0:
         raise ValueError("the key head count must divide the query head count")
+    if any(t.device != Q1.device for t in (K1, Q2, K2)):
+        raise ValueError("Q1, K1, Q2 and K2 must be on one device")
+
+
+def _check_tensor(name, t, shape, dtype, device):
+    """Outputs and per-row inputs are written or read as dense arrays of the
+    given shape: anything else would send the kernels out of bounds."""
+    if not isinstance(t, torch.Tensor) or t.device != device:
+        raise ValueError(f"{name} must be a tensor on {device}")
+    if t.dtype != dtype or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)}, got "
+                         f"{t.dtype} {tuple(t.shape)}{'' if t.is_contiguous() else ' (not contiguous)'}")
+
+
+def _check_workspace(workspace, nbytes, device):
+    """None allocates one; a caller's workspace must be a large enough
+    contiguous uint8 tensor on the inputs' device (it is never replaced)."""
+    if workspace is None:
+        return new_workspace(nbytes, device)
+    if not isinstance(workspace, torch.Tensor) or workspace.device != device or workspace.dtype != torch.uint8 \
+            or not workspace.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous uint8 tensor on {device}")
+    if workspace.numel() < nbytes:
+        raise ValueError(f"workspace holds {workspace.numel()} bytes; this call needs {nbytes} (see fwd_plan / bwd_plan)")
+    return workspace
 
 
 def _opts(num_splits=0, bwd_mode=0, wait_limit_ns=0, debug_flags=0, grad_bf16=0):
@@ -177,8 +202,9 @@ def kl_fwd(Q1, K1, Q2, K2, causal=False, scale=None, num_splits=0, workspace=Non
     B, H, Nq, _ = Q1.shape
     if out is None:
         out = tuple(torch.empty((B, H, Nq), dtype=torch.float32, device=Q1.device) for _ in range(3))
-    if workspace is None or workspace.numel() < plan.workspace_bytes:
-        workspace = new_workspace(plan.workspace_bytes, Q1.device)
+    for name, t in zip(("KL", "LSE1", "LSE2"), out):
+        _check_tensor(name, t, (B, H, Nq), torch.float32, Q1.device)
+    workspace = _check_workspace(workspace, plan.workspace_bytes, Q1.device)
     KL, L1, L2 = out
     rc = lib.streamkl_fwd(ctypes.byref(shape), _ptr(Q1), _ptr(K1), _ptr(Q2), _ptr(K2),
                           ctypes.c_float(0.0 if scale is None else float(scale)), int(bool(causal)), _ptr(KL),
@@ -204,16 +230,13 @@ def kl_bwd(setting, g, Q1, K1, Q2, K2, KL, LSE1, LSE2, causal=False, scale=None,
     B, H, Nq, d = Q1.shape
     Nk = K1.shape[2]
     for name, t in (("g", g), ("KL", KL), ("LSE1", LSE1), ("LSE2", LSE2)):
-        if t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != (B, H, Nq):
-            raise ValueError(f"{name} must be contiguous float32 [B, H, Nq]")
+        _check_tensor(name, t, (B, H, Nq), torch.float32, Q1.device)
     if out is None:
         out = (torch.empty((B, H, Nq, d), dtype=grad_dtype, device=Q1.device),
                torch.empty((B, K1.shape[1], Nk, d), dtype=grad_dtype, device=Q1.device))
-    for t in out:
-        if t.dtype != grad_dtype or not t.is_contiguous():
-            raise ValueError("gradient outputs must be contiguous tensors of grad_dtype")
-    if workspace is None or workspace.numel() < plan.workspace_bytes:
-        workspace = new_workspace(plan.workspace_bytes, Q1.device)
+    _check_tensor("dQ", out[0], (B, H, Nq, d), grad_dtype, Q1.device)
+    _check_tensor("dK", out[1], (B, K1.shape[1], Nk, d), grad_dtype, Q1.device)
+    workspace = _check_workspace(workspace, plan.workspace_bytes, Q1.device)
     dQ, dK = out
     rc = lib.streamkl_bwd(ctypes.byref(shape), int(setting), _ptr(g), _ptr(Q1), _ptr(K1), _ptr(Q2), _ptr(K2),
                           _ptr(KL), _ptr(LSE1), _ptr(LSE2), ctypes.c_float(0.0 if scale is None else float(scale)),

@@ -138,7 +138,7 @@ def gpu_id(dev):
 
 
 def config_for(w, world):
-    return {"workload": f"{w.name}: B={w.B} H={w.H} N_Q={w.Nq} N_K={w.Nk} d={w.d} "
+    return {"workload": f"{w.name}: B={w.B} H={w.H}{f' H_kv={w.H_kv}' if w.H_kv else ''} N_Q={w.Nq} N_K={w.Nk} d={w.d} "
                         f"{'causal' if w.causal else 'non-causal'}, "
                         + ("fwd only (Split-K decode) per step" if w.fwd_only else
                            "fwd + bwd setting 1 + bwd setting 2 per step"),
@@ -207,7 +207,7 @@ def run_gpu(args):
     f32 = dict(dtype=torch.float32, device=dev)
     KL, L1, L2 = (torch.empty((B, H, Nq), **f32) for _ in range(3))
     dQ = torch.empty((B, H, Nq, d), **f32) if not w.fwd_only else None
-    dK = torch.empty((B, H, Nk, d), **f32) if not w.fwd_only else None
+    dK = torch.empty((B, K1.shape[1], Nk, d), **f32) if not w.fwd_only else None  # key heads (H_kv)
     fplan = streamkl.fwd_plan(Q1, K1, causal=w.causal)
     bplan1 = streamkl.bwd_plan(Q1, K1, 1, causal=w.causal)
     bplan2 = streamkl.bwd_plan(Q1, K1, 2, causal=w.causal)

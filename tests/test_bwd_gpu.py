@@ -252,3 +252,32 @@ def test_softmax_scale_other_than_the_default(scale, mode):
         rdQ, rdK = oracle.bwd(setting, g, Q1, K1, Q2, K2, causal=causal, scale=scale)
         assert_grad(dQ, rdQ, f"dQ (setting {setting}, scale {scale})")
         assert_grad(dK, rdK, f"dK (setting {setting}, scale {scale})")
+
+
+def test_binding_rejects_mis_shaped_buffers():
+    """Outputs, per-row inputs and the workspace are checked against the
+    problem's shapes before anything launches (a short buffer would be written
+    past its end)."""
+    Q1, K1, Q2, K2 = make_qk(1, 4, 130, 200, 64, 0.4, seed=3, device=DEV, H_kv=2)
+    KL, L1, L2 = streamkl.kl_fwd(Q1, K1, Q2, K2)
+    g = torch.ones((1, 4, 130), device=DEV)
+    f32 = dict(dtype=torch.float32, device=DEV)
+    with pytest.raises(ValueError):
+        streamkl.kl_fwd(Q1, K1, Q2, K2, out=(torch.empty((1, 4, 129), **f32), L1, L2))
+    with pytest.raises(ValueError):
+        streamkl.kl_fwd(Q1, K1, Q2, K2, out=(KL, L1, torch.empty((1, 4, 130), dtype=torch.float16, device=DEV)))
+    with pytest.raises(ValueError):
+        streamkl.kl_fwd(Q1, K1, Q2, K2, workspace=torch.zeros(1 << 20, dtype=torch.float32, device=DEV))
+    with pytest.raises(ValueError):  # smaller than the plan asks for
+        streamkl.kl_fwd(Q1, K1, Q2, K2, workspace=torch.zeros(16, dtype=torch.uint8, device=DEV))
+    with pytest.raises(ValueError):  # dK has the key heads (2), not the query heads (4)
+        streamkl.kl_bwd(1, g, Q1, K1, Q2, K2, KL, L1, L2,
+                        out=(torch.empty((1, 4, 130, 64), **f32), torch.empty((1, 1, 200, 64), **f32)))
+    with pytest.raises(ValueError):
+        streamkl.kl_bwd(1, g[:, :, :100], Q1, K1, Q2, K2, KL, L1, L2)
+    with pytest.raises(ValueError):
+        streamkl.kl_bwd(1, g.cpu(), Q1, K1, Q2, K2, KL, L1, L2)
+    dQ, dK = streamkl.kl_bwd(1, g, Q1, K1, Q2, K2, KL, L1, L2,
+                             out=(torch.empty((1, 4, 130, 64), **f32), torch.empty((1, 2, 200, 64), **f32)))
+    torch.cuda.synchronize()
+    assert torch.isfinite(dQ).all() and torch.isfinite(dK).all()

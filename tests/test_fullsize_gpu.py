@@ -162,3 +162,44 @@ def test_decode_shaped_backward_both_settings():
     w = WORKLOADS["decode_bwd_q16_k128k"]
     run_workload(w.name, (1, 2), heads=(0, 77, w.B * w.H - 1), rows_per_head=2 * w.Nq, key_tail=w.Nk,
                  keys_per_head=32)
+
+
+def test_64k_causal_shared_keys_forward_and_setting1():
+    """64K causal, 32 query heads on 8 key heads: sampled rows of KL, LSE and
+    dQ of query heads, and dK of the last keys of a key head, which sums the
+    gradients of its 4 query heads."""
+    w = WORKLOADS["64k_causal_gqa"]
+    inputs = make_workload(w, device=DEV)
+    Q1, K1, Q2, K2 = inputs
+    group = w.H // w.H_kv
+    KL, L1, L2 = streamkl.kl_fwd(*inputs, causal=w.causal)
+    torch.cuda.synchronize()
+
+    def views(h):  # query head h with the key head it shares
+        return [Q1[0, h][None, None], K1[0, h // group][None, None], Q2[0, h][None, None],
+                K2[0, h // group][None, None]]
+
+    rng = np.random.default_rng(w.seed)
+    for h in (0, 13, 31):
+        rows = rows_for_head(w.Nq, 32, rng)
+        rKL, rL1, rL2 = oracle.fwd_rows(*views(h), rows, causal=w.causal)
+        idx = torch.as_tensor(rows, device=DEV)
+        assert_lse(L1[0, h][idx], rL1, f"LSE1 head {h}")
+        assert_lse(L2[0, h][idx], rL2, f"LSE2 head {h}")
+        assert_kl(KL[0, h][idx], rKL, f"KL head {h}")
+    g = make_g(w.B, w.H, w.Nq, w.g_value, device=DEV)
+    dQ, dK = streamkl.kl_bwd(1, g, *inputs, KL, L1, L2, causal=w.causal)
+    torch.cuda.synchronize()
+    assert dK.shape[1] == w.H_kv
+    gq, rq = [], []
+    for h in (0, 13, 31):
+        rows = rows_for_head(w.Nq, 16, rng)
+        rq.append(oracle.bwd_dq_rows(1, g[0, h][None, None], *views(h), rows, causal=w.causal))
+        gq.append(dQ[0, h][torch.as_tensor(rows, device=DEV)])
+    assert_grad(torch.cat(gq), np.concatenate(rq), "dQ rows, shared keys (setting 1)")
+    hk = 3
+    keys = np.array(sorted(set(rng.integers(w.Nk - 512, w.Nk, size=16).tolist()) | {w.Nk - 512, w.Nk - 1}),
+                    dtype=np.int64)
+    rk = sum(oracle.bwd_dk_keys(1, g[0, h][None, None], *views(h), keys, causal=w.causal)
+             for h in range(hk * group, (hk + 1) * group))
+    assert_grad(dK[0, hk][torch.as_tensor(keys, device=DEV)], rk, "dK keys of a shared key head (setting 1)")
