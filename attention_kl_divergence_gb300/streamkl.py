@@ -260,7 +260,11 @@ class AttentionKL(torch.autograd.Function):
     """Per-row KL(softmax(Q1 K1^T s) || softmax(Q2 K2^T s)) with a recompute
     backward.  Gradients flow to the student (setting 1) or the teacher
     (setting 2), chosen by which inputs require grad; the other side gets
-    None.  Both sides at once is not offered by this function."""
+    None.  When both sides require grad, both settings run, one backward pass
+    each (no fused joint pass: it would not be faster on this hardware).
+    Together they are the gradient of KL with respect to all four inputs: each
+    setting differentiates through one side's distribution with the other
+    side's held fixed.  Gradients come back in bf16, like the inputs."""
 
     @staticmethod
     def forward(ctx, Q1, K1, Q2, K2, causal=False, scale=None):
@@ -274,13 +278,13 @@ class AttentionKL(torch.autograd.Function):
         Q1, K1, Q2, K2, KL, L1, L2 = ctx.saved_tensors
         student = ctx.needs_input_grad[2] or ctx.needs_input_grad[3]
         teacher = ctx.needs_input_grad[0] or ctx.needs_input_grad[1]
-        if student and teacher:
-            raise NotImplementedError("gradients to both teacher and student in one backward")
         if not (student or teacher):
             return (None,) * 6
-        setting = 1 if student else 2
-        dQ, dK = kl_bwd(setting, gKL.float().contiguous(), Q1, K1, Q2, K2, KL, L1, L2, causal=ctx.causal,
-                        scale=ctx.scale, grad_dtype=torch.bfloat16)
-        if setting == 1:
-            return None, None, dQ, dK, None, None
-        return dQ, dK, None, None, None, None
+        g = gKL.float().contiguous()
+        grads = [None] * 6
+        for setting, want, slot in ((1, student, 2), (2, teacher, 0)):
+            if want:
+                dQ, dK = kl_bwd(setting, g, Q1, K1, Q2, K2, KL, L1, L2, causal=ctx.causal, scale=ctx.scale,
+                                grad_dtype=torch.bfloat16)
+                grads[slot], grads[slot + 1] = dQ, dK
+        return tuple(grads)

@@ -281,3 +281,21 @@ def test_binding_rejects_mis_shaped_buffers():
                              out=(torch.empty((1, 4, 130, 64), **f32), torch.empty((1, 2, 200, 64), **f32)))
     torch.cuda.synchronize()
     assert torch.isfinite(dQ).all() and torch.isfinite(dK).all()
+
+
+def test_autograd_both_sides():
+    """Teacher and student both require grad: each side gets its own
+    setting's gradient (setting 1 holds P1 fixed, setting 2 holds P2 fixed)."""
+    Q1, K1, Q2, K2 = make_qk(1, 2, 180, 250, 64, 0.5, seed=4, device=DEV)
+    for t in (Q1, K1, Q2, K2):
+        t.requires_grad_(True)
+    KL = streamkl.AttentionKL.apply(Q1, K1, Q2, K2, False, None)
+    g = torch.rand((1, 2, 180), device=DEV) + 0.5
+    (KL * g).sum().backward()
+    det = [t.detach() for t in (Q1, K1, Q2, K2)]
+    r1 = oracle.bwd(1, g, *det, causal=False)
+    r2 = oracle.bwd(2, g, *det, causal=False)
+    assert_grad(Q2.grad.float(), r1[0], "dQ2 (both sides)")
+    assert_grad(K2.grad.float(), r1[1], "dK2 (both sides)")
+    assert_grad(Q1.grad.float(), r2[0], "dQ1 (both sides)")
+    assert_grad(K1.grad.float(), r2[1], "dK1 (both sides)")
