@@ -143,10 +143,11 @@ struct BwdPlan {
 
 // Mode choice.  The pages use the fused kernel (dQ through atomics) while the
 // float32 dQ buffer fits in L2 and separate kernels beyond.  Measured on
-// GB300 the fused kernel is faster at every size tried (8K causal 2.0 vs
-// 2.5 ms, 64K causal 108 vs 138 ms: the split pays a second recompute of both
-// score tiles, which costs more than the L2 reductions), so the automatic
-// choice is always fused; the split stays selectable.
+// GB300 the fused kernel is faster at every size tried (setting 1: 8K causal
+// 1.21 vs 2.14 ms, 64K causal 71.0 vs 117.8 ms: the split pays a second
+// recompute of both score tiles, which costs more than the L2 reductions), so
+// the automatic choice is fused unless every query row of a key head fits one
+// CTA's 16 columns (the key-split kernel); the split stays selectable.
 streamkl_status plan_bwd(const streamkl_shape* s, int setting, int causal, const streamkl_options* opt,
                          BwdPlan* pl) {
     streamkl_status st = check_shape(s, causal);
@@ -352,6 +353,16 @@ streamkl_status streamkl_bwd_plan(const streamkl_shape* shape, int setting, int 
     return STREAMKL_OK;
 }
 
+size_t streamkl_fwd_workspace_bytes(const streamkl_shape* shape, int causal) {
+    FwdPlan pl{};
+    return plan_fwd(shape, causal, nullptr, &pl) == STREAMKL_OK ? pl.ws_bytes : 0;
+}
+
+size_t streamkl_bwd_workspace_bytes(const streamkl_shape* shape, int setting, int causal) {
+    BwdPlan pl{};
+    return plan_bwd(shape, setting, causal, nullptr, &pl) == STREAMKL_OK ? pl.ws_bytes : 0;
+}
+
 streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const float* g, const void* Q1,
                              const void* K1, const void* Q2, const void* K2, const float* KL, const float* LSE1,
                              const float* LSE2, float scale, int causal, void* dQ, void* dK, void* workspace,
@@ -458,31 +469,35 @@ streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const flo
 // Forward without any allocation: the scratch lives in this file-scope device
 // array (every GPU that loads the library holds it until the process exits).
 // Host code only ever sees the array's host-side stand-in; its device address
-// comes from cudaGetSymbolAddress, looked up once per device below.
+// comes from cudaGetSymbolAddress, with the device of the call current.
 // ---------------------------------------------------------------------------
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = STREAMKL_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (set-up on the
-// first call per device, with that device current).
+// Device address of the scratch array on the current device.  It is looked up
+// on every call (a host-side table lookup once the device code is loaded, and
+// no allocation), so no address can outlive the context it belongs to: after
+// a cudaDeviceReset the next call resolves the array in the new context.  The
+// first call on a device also loads the library's device code there.
 streamkl_status noalloc_scratch(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return STREAMKL_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return STREAMKL_ERR_CUDA;
-        g_noalloc_ptr[dev] = ptr;
-    }
-    *out = g_noalloc_ptr[dev];
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return STREAMKL_ERR_CUDA;
+    *out = ptr;
     return STREAMKL_OK;
+}
+
+// Read the device error word at `word_dev` after `stream` drains, clear it if
+// set, and map it to a status (shared by both status queries).
+streamkl_status read_error_word(void* word_dev, cudaStream_t s, uint32_t* device_error) {
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, word_dev, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return STREAMKL_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+    if (word != 0 && cudaMemsetAsync(word_dev, 0, sizeof(word), s) != cudaSuccess) return STREAMKL_ERR_CUDA;
+    if (device_error) *device_error = word;
+    return word ? STREAMKL_ERR_TIMEOUT : STREAMKL_OK;
 }
 
 }  // namespace
@@ -508,14 +523,14 @@ streamkl_status streamkl_fwd_noalloc(const streamkl_shape* shape, const void* Q1
 
 streamkl_status streamkl_workspace_status(void* workspace, streamkl_stream_t stream, uint32_t* device_error) {
     if (!workspace) return STREAMKL_ERR_INVALID_ARG;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    uint32_t word = 0;
-    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return STREAMKL_ERR_CUDA;
-    if (cudaStreamSynchronize(s) != cudaSuccess) return STREAMKL_ERR_CUDA;
-    if (word != 0 && cudaMemsetAsync(workspace, 0, sizeof(word), s) != cudaSuccess) return STREAMKL_ERR_CUDA;
-    if (device_error) *device_error = word;
-    return word ? STREAMKL_ERR_TIMEOUT : STREAMKL_OK;
+    return read_error_word(workspace, reinterpret_cast<cudaStream_t>(stream), device_error);
+}
+
+streamkl_status streamkl_noalloc_status(streamkl_stream_t stream, uint32_t* device_error) {
+    void* scratch = nullptr;
+    streamkl_status st = noalloc_scratch(&scratch);
+    if (st != STREAMKL_OK) return st;
+    return read_error_word(scratch, reinterpret_cast<cudaStream_t>(stream), device_error);
 }
 
 }  // extern "C"

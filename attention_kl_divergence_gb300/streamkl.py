@@ -53,7 +53,8 @@ class StreamKLError(RuntimeError):
 
 
 EXPORTED = ("streamkl_fwd_plan", "streamkl_fwd", "streamkl_bwd_plan", "streamkl_bwd", "streamkl_workspace_status",
-            "streamkl_status_string", "streamkl_version", "streamkl_fwd_noalloc")
+            "streamkl_status_string", "streamkl_version", "streamkl_fwd_noalloc", "streamkl_noalloc_status",
+            "streamkl_fwd_workspace_bytes", "streamkl_bwd_workspace_bytes")
 
 _lock = threading.Lock()
 _lib = None
@@ -82,10 +83,16 @@ def load(build_if_stale: bool = True):
         lib.streamkl_bwd.argtypes = [sp, I, P, P, P, P, P, P, P, P, F, I, P, P, P, Z, op, P]
         lib.streamkl_workspace_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
         lib.streamkl_fwd_noalloc.argtypes = [sp, P, P, P, P, F, I, P, P, P, op, P]
+        lib.streamkl_noalloc_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+        lib.streamkl_fwd_workspace_bytes.argtypes = [sp, I]
+        lib.streamkl_bwd_workspace_bytes.argtypes = [sp, I, I]
+        lib.streamkl_fwd_workspace_bytes.restype = Z
+        lib.streamkl_bwd_workspace_bytes.restype = Z
         lib.streamkl_status_string.argtypes = [I]
         lib.streamkl_status_string.restype = ctypes.c_char_p
         for name in ("streamkl_fwd_plan", "streamkl_fwd", "streamkl_bwd_plan", "streamkl_bwd",
-                     "streamkl_workspace_status", "streamkl_version", "streamkl_fwd_noalloc"):
+                     "streamkl_workspace_status", "streamkl_version", "streamkl_fwd_noalloc",
+                     "streamkl_noalloc_status"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -174,6 +181,29 @@ def bwd_plan(Q1, K1, setting, causal=False, mode=BWD_AUTO, grad_dtype=torch.floa
                                     ctypes.byref(_opts(num_splits, mode, grad_bf16=_grad_flag(grad_dtype))),
                                     ctypes.byref(plan)), "streamkl_bwd_plan")
     return plan
+
+
+def fwd_workspace_bytes(Q1, K1, causal=False) -> int:
+    """streamkl_fwd_workspace_bytes: the forward's workspace with default options (0 = invalid shape)."""
+    return int(load().streamkl_fwd_workspace_bytes(ctypes.byref(make_shape(Q1, K1)), int(bool(causal))))
+
+
+def bwd_workspace_bytes(Q1, K1, setting, causal=False) -> int:
+    """streamkl_bwd_workspace_bytes: the backward's workspace with default options (0 = invalid)."""
+    return int(load().streamkl_bwd_workspace_bytes(ctypes.byref(make_shape(Q1, K1)), int(setting),
+                                                   int(bool(causal))))
+
+
+def noalloc_status(device=None) -> int:
+    """streamkl_noalloc_status: synchronise the current stream of ``device`` and
+    return (and clear) the device error word of the allocation-free forward's
+    built-in scratch (0 when no bounded wait gave up)."""
+    word = ctypes.c_uint32(0)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    rc = load().streamkl_noalloc_status(_stream(dev), ctypes.byref(word))
+    if rc not in (OK, ERR_TIMEOUT):
+        _raise(rc, "streamkl_noalloc_status")
+    return int(word.value)
 
 
 def _grad_flag(grad_dtype):

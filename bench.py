@@ -14,12 +14,16 @@ through the C ABI with host buffers, clocks, and the float64 CPU oracle timed
 on a bounded sample of the same workload.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-Under torchrun every rank runs its own copy of the workload (heads are
-independent, no collective on the data path): weak scaling.
+Under torchrun the heads of the one problem are split across the ranks (heads
+are independent problems, so there is no collective on the data path): strong
+scaling, the value is the whole problem's work over the slowest rank's time.
+After the headline step the same run times the N_Q=1, N_K=512K Split-K decode
+forward (B=4, H=32, d=128), HBM-bound, with its own clock sample.
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -35,31 +39,49 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from attention_kl_divergence_gb300 import WORKLOADS, make_g, make_workload  # noqa: E402
-from attention_kl_divergence_gb300.dist import barrier, env as dist_env, init as init_dist, max_over_ranks  # noqa: E402
+from attention_kl_divergence_gb300.dist import (barrier, env as dist_env, head_range, init as init_dist,  # noqa: E402
+                                                max_over_ranks)
 
 WORKLOAD = "64k_causal"
+DECODE_WORKLOAD = "decode_q1_k512k"
 METRIC = "fwd/bwd TFLOP/s and ms at 64K causal, fraction of GB300 BF16 tensor peak"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from ncu
-# (dram__bytes_read.sum + dram__bytes_write.sum) on the same command
-# (profiles/dram_64k_causal.md).  Keyed by (workload, pass) and valid only for the kernel
-# version they were taken on: reset to None whenever that kernel changes.
+# DRAM bytes (read + write) per launch of a kernel, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), with the hash of the kernel
+# source files it was taken on: a table entry whose hash differs from the
+# sources being run is stale and reported as null.
+KERNEL_SOURCES = {
+    "fwd": ("fwd.cu", "common.cuh", "ptx.cuh"),
+    "bwd": ("bwd.cu", "bwd_common.cuh", "common.cuh", "ptx.cuh"),
+}
 TRAFFIC = {
-    ("64k_causal", "fwd"): 2.17e9 + 0.038e9,
-    ("64k_causal", "bwd_setting1"): 3.350e9 + 2.250e9,
-    ("64k_causal", "bwd_setting2"): 3.364e9 + 2.252e9,
-    ("decode_bwd_q16_k128k", "bwd_setting1"): 8.81e9 + 8.54e9,
-    ("decode_bwd_q16_k128k", "bwd_setting2"): 8.80e9 + 8.54e9,
+    ("64k_causal", "fwd"): (2.17e9 + 0.036e9, "fwd", "98b687add18abd65"),
+    ("64k_causal", "bwd_setting1"): (3.35e9 + 2.25e9, "bwd", "6341bcd50b264510"),
+    ("64k_causal", "bwd_setting2"): (3.36e9 + 2.25e9, "bwd", "6341bcd50b264510"),
 }
 
 
-BWD_MODE_NAMES = {2: "fused", 3: "split", 4: "keysplit"}  # plan paths of the backward
+def source_hash(kind):
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "attention_kl_divergence_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def traffic_for(workload, which):
-    return TRAFFIC.get((workload, which))
+    """Measured DRAM bytes per launch, or None when there is no capture of the
+    kernel as it is built now."""
+    entry = TRAFFIC.get((workload, which))
+    if entry is None:
+        return None
+    nbytes, kind, digest = entry
+    return nbytes if source_hash(kind) == digest else None
+
+
+BWD_MODE_NAMES = {2: "fused", 3: "split", 4: "keysplit"}  # plan paths of the backward
 
 
 def load_peaks():
@@ -142,7 +164,25 @@ def config_for(w, world):
                         f"{'causal' if w.causal else 'non-causal'}, "
                         + ("fwd only (Split-K decode) per step" if w.fwd_only else
                            "fwd + bwd setting 1 + bwd setting 2 per step"),
-            "l2": "256 MB write between steps", "parallelism": f"heads-independent replicas x{world}"}
+            "l2": "256 MB write between steps (inputs exceed L2 as well)",
+            "parallelism": f"heads split across {world} GPU(s), no collective on the data path"}
+
+
+def rank_heads(w, rank, world):
+    """[start, stop) of the flat key heads (b * H_kv + hk) this rank owns; the
+    query heads of a key head's group go with it.  Shards differ by at most
+    one key head and together cover every head exactly once."""
+    units = w.B * (w.H_kv or w.H)
+    if world > units:
+        raise ValueError(f"{world} ranks for {units} heads")
+    return head_range(units, rank, world)
+
+
+def shard(t, start, stop, group=1):
+    """Heads [start*group, stop*group) of a [B, H, N, ...] tensor as a
+    contiguous [1, n, N, ...] view (B and H flattened)."""
+    B, H = t.shape[:2]
+    return t.reshape(B * H, *t.shape[2:])[start * group:stop * group].unsqueeze(0)
 
 
 def flush_l2(buf):
@@ -201,13 +241,28 @@ def run_gpu(args):
     init_dist(ws_, "nccl")
     w = WORKLOADS[args.workload]
     peaks, peak_src = load_peaks()
-    Q1, K1, Q2, K2 = make_workload(w, device=dev)
-    g = make_g(w.B, w.H, w.Nq, w.g_value, device=dev)
-    B, H, Nq, Nk, d = w.B, w.H, w.Nq, w.Nk, w.d
+    group = w.H // (w.H_kv or w.H)
+    start, stop = rank_heads(w, rank, ws_)
+    # the whole problem is drawn from its seed on every rank; each rank keeps its heads
+    full = make_workload(w, device=dev)
+    Q1, K1, Q2, K2 = (shard(t, start, stop, group if k % 2 == 0 else 1) for k, t in enumerate(full))
+    Q1, K1, Q2, K2 = (t.clone() for t in (Q1, K1, Q2, K2))
+    del full
+    Hq, Hk = Q1.shape[1], K1.shape[1]
+    g = make_g(1, Hq, w.Nq, w.g_value, device=dev)
+    Nq, Nk, d = w.Nq, w.Nk, w.d
     f32 = dict(dtype=torch.float32, device=dev)
-    KL, L1, L2 = (torch.empty((B, H, Nq), **f32) for _ in range(3))
-    dQ = torch.empty((B, H, Nq, d), **f32) if not w.fwd_only else None
-    dK = torch.empty((B, K1.shape[1], Nk, d), **f32) if not w.fwd_only else None  # key heads (H_kv)
+    with_bwd = not w.fwd_only
+
+    def outputs():
+        o = {"KL": torch.empty((1, Hq, Nq), **f32), "LSE1": torch.empty((1, Hq, Nq), **f32),
+             "LSE2": torch.empty((1, Hq, Nq), **f32)}
+        if with_bwd:  # setting 1 -> student gradients, setting 2 -> teacher gradients
+            o.update(dQ2=torch.empty((1, Hq, Nq, d), **f32), dK2=torch.empty((1, Hk, Nk, d), **f32),
+                     dQ1=torch.empty((1, Hq, Nq, d), **f32), dK1=torch.empty((1, Hk, Nk, d), **f32))
+        return o
+
+    out = outputs()
     fplan = streamkl.fwd_plan(Q1, K1, causal=w.causal)
     bplan1 = streamkl.bwd_plan(Q1, K1, 1, causal=w.causal)
     bplan2 = streamkl.bwd_plan(Q1, K1, 2, causal=w.causal)
@@ -215,13 +270,16 @@ def run_gpu(args):
     l2_flush = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def fwd():
-        streamkl.kl_fwd(Q1, K1, Q2, K2, causal=w.causal, workspace=wsp, out=(KL, L1, L2))
+    def step_on(ins, o):
+        q1, k1, q2, k2, gg = ins
+        streamkl.kl_fwd(q1, k1, q2, k2, causal=w.causal, workspace=wsp, out=(o["KL"], o["LSE1"], o["LSE2"]))
+        if with_bwd:
+            streamkl.kl_bwd(1, gg, q1, k1, q2, k2, o["KL"], o["LSE1"], o["LSE2"], causal=w.causal, workspace=wsp,
+                            out=(o["dQ2"], o["dK2"]))
+            streamkl.kl_bwd(2, gg, q1, k1, q2, k2, o["KL"], o["LSE1"], o["LSE2"], causal=w.causal, workspace=wsp,
+                            out=(o["dQ1"], o["dK1"]))
 
-    def bwd(setting):
-        streamkl.kl_bwd(setting, g, Q1, K1, Q2, K2, KL, L1, L2, causal=w.causal, workspace=wsp, out=(dQ, dK))
-
-    with_bwd = not w.fwd_only
+    ins = (Q1, K1, Q2, K2, g)
     launches_per_step = fplan.launches + ((bplan1.launches + bplan2.launches) if with_bwd else 0)
     adds_dq = (streamkl.PATH_BWD_FUSED, streamkl.PATH_BWD_KEYSPLIT)
     if with_bwd and bplan1.path in adds_dq:
@@ -229,14 +287,8 @@ def run_gpu(args):
     if with_bwd and bplan2.path in adds_dq:
         launches_per_step -= 1
 
-    def step():
-        fwd()
-        if with_bwd:
-            bwd(1)
-            bwd(2)
-
     for _ in range(args.warmup):
-        step()
+        step_on(ins, out)
     torch.cuda.synchronize()
     if streamkl.workspace_status(wsp):
         raise RuntimeError("device error word set during warm-up")
@@ -249,13 +301,15 @@ def run_gpu(args):
             flush_l2(l2_flush)
             e = ev[k]
             e[0].record(stream)
-            fwd()
+            streamkl.kl_fwd(Q1, K1, Q2, K2, causal=w.causal, workspace=wsp, out=(out["KL"], out["LSE1"], out["LSE2"]))
             e[1].record(stream)
             if with_bwd:
-                bwd(1)
+                streamkl.kl_bwd(1, g, Q1, K1, Q2, K2, out["KL"], out["LSE1"], out["LSE2"], causal=w.causal,
+                                workspace=wsp, out=(out["dQ2"], out["dK2"]))
             e[2].record(stream)
             if with_bwd:
-                bwd(2)
+                streamkl.kl_bwd(2, g, Q1, K1, Q2, K2, out["KL"], out["LSE1"], out["LSE2"], causal=w.causal,
+                                workspace=wsp, out=(out["dQ1"], out["dK1"]))
             e[3].record(stream)
         torch.cuda.synchronize()
     barrier(ws_)
@@ -267,23 +321,25 @@ def run_gpu(args):
     step_ms = sum(e[0].elapsed_time(e[3]) for e in ev) / args.steps
     step_ms = max_over_ranks(step_ms, ws_, dev)
 
-    pairs = w.visible_pairs() * B * H
+    # work of the whole problem (every rank's heads) and of this rank's share
+    pairs_all = w.visible_pairs() * w.B * w.H
+    pairs = w.visible_pairs() * Hq
     f_fwd, f_bwd = 4 * d * pairs, 8 * d * pairs
-    step_flops = f_fwd + (2 * f_bwd if with_bwd else 0)
-    value = step_flops * ws_ / (step_ms * 1e-3) / 1e12
+    step_flops_all = 4 * d * pairs_all + (2 * 8 * d * pairs_all if with_bwd else 0)
+    value = step_flops_all / (step_ms * 1e-3) / 1e12
     peak_tf = peaks["bf16_tflops"]
     peak_sus = peaks.get("bf16_tflops_sustained", PEAKS_FALLBACK["bf16_tflops_sustained"])
+    share = (stop - start) / (w.B * (w.H_kv or w.H))
+    fwd_bytes, bwd_bytes = w.fwd_bytes() * share, w.bwd_bytes() * share
     kernels = {"fwd": {"ms": fwd_ms, "tflops": f_fwd / fwd_ms / 1e9, "frac_bf16_peak": f_fwd / fwd_ms / 1e9 / peak_tf,
                        "frac_bf16_sustained": f_fwd / fwd_ms / 1e9 / peak_sus,
-                       "gbs": w.fwd_bytes() / fwd_ms / 1e6, "frac_hbm_peak": w.fwd_bytes() / fwd_ms / 1e6 /
-                       peaks["hbm_gbs"], "path": "tile" if fplan.path == 0 else "decode",
-                       "splits": fplan.num_splits}}
+                       "gbs": fwd_bytes / fwd_ms / 1e6, "frac_hbm_peak": fwd_bytes / fwd_ms / 1e6 / peaks["hbm_gbs"],
+                       "path": "tile" if fplan.path == 0 else "decode", "splits": fplan.num_splits}}
     if with_bwd:
         for name, ms, plan in (("bwd_setting1", b1_ms, bplan1), ("bwd_setting2", b2_ms, bplan2)):
             kernels[name] = {"ms": ms, "tflops": f_bwd / ms / 1e9, "frac_bf16_peak": f_bwd / ms / 1e9 / peak_tf,
                              "frac_bf16_sustained": f_bwd / ms / 1e9 / peak_sus,
-                             "gbs": w.bwd_bytes() / ms / 1e6, "frac_hbm_peak": w.bwd_bytes() / ms / 1e6 /
-                             peaks["hbm_gbs"],
+                             "gbs": bwd_bytes / ms / 1e6, "frac_hbm_peak": bwd_bytes / ms / 1e6 / peaks["hbm_gbs"],
                              "mode": BWD_MODE_NAMES[plan.path]}
     # Roofline of the dominant kernel (largest share of the step), timed live
     # with CUDA events around its call on the launching stream.  Forward call =
@@ -303,77 +359,76 @@ def run_gpu(args):
     names = {"fwd": "fwd_tile_kernel" if fplan.path == 0 else "fwd_decode_kernel + combine_kernel",
              "bwd_setting1": bwd_name(bplan1, 1), "bwd_setting2": bwd_name(bplan2, 2)}
     top = max(kernels, key=lambda k: kernels[k]["ms"])
+    # traffic is per launch of the full problem on one GPU; a shard's launch moves its share
+    traffic = traffic_for(w.name, top)
+    traffic = traffic * share if traffic is not None else None
     # a decode-shaped problem (at most 16 query rows) moves ~1 (N_Q = 1) to ~16 flops per
     # byte in either direction, far below the ridge: HBM bounds its kernels
     if Nq <= 16:
-        nbytes = w.fwd_bytes() if top == "fwd" else w.bwd_bytes()
+        nbytes = fwd_bytes if top == "fwd" else bwd_bytes
         achieved = nbytes / kernels[top]["ms"] / 1e6
         roofline = {"kernel": names[top], "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_for(w.name, top),
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                     "share_of_step": kernels[top]["ms"] / step_ms, "bytes_per_launch": nbytes,
                     "peak_source": f"hbm_gbs ({peak_src})"}
     else:
         flops_top = f_fwd if top == "fwd" else f_bwd
         achieved = flops_top / kernels[top]["ms"] / 1e9
-        # The kernel is timed inside the step: in a long step (tens of ms and more of
-        # back-to-back tensor work) the GPU sits at its power cap, where the measured
-        # sustained GEMM rate is the ceiling; a short step runs at the burst rate.
-        long_step = step_ms >= 50.0
-        peak = peak_sus if long_step else peak_tf
-        roofline = {"kernel": names[top], "bound": "tensor", "achieved": achieved, "peak": peak,
-                    "unit": "TFLOP/s", "frac": achieved / peak, "frac_of_burst_peak": achieved / peak_tf,
-                    "traffic": traffic_for(w.name, top),
+        # frac: of the measured burst GEMM rate; the sustained (seconds-long, at the
+        # power cap) rate is reported beside it
+        roofline = {"kernel": names[top], "bound": "tensor", "achieved": achieved, "peak": peak_tf,
+                    "unit": "TFLOP/s", "frac": achieved / peak_tf, "frac_sustained": achieved / peak_sus,
+                    "peak_sustained": peak_sus, "traffic": traffic,
+                    "traffic_kernel_hash": source_hash("fwd" if top == "fwd" else "bwd"),
                     "share_of_step": kernels[top]["ms"] / step_ms, "flops_per_launch": flops_top,
-                    "peak_source": (f"bf16_tflops_sustained ({peak_src}; timed inside a {step_ms:.0f} ms step)"
-                                    if long_step else f"bf16_tflops ({peak_src}, burst)")}
+                    "peak_source": f"bf16_tflops ({peak_src}, burst)"}
 
     # ---------------- end to end through the C ABI with host buffers
-    pin = dict(pin_memory=True)
-    hQ1, hK1, hQ2, hK2 = (t.cpu().pin_memory() for t in (Q1, K1, Q2, K2))
-    hg = g.cpu().pin_memory()
-    hKL = torch.empty((B, H, Nq), dtype=torch.float32, **pin)
-    h2d = sum(t.numel() * t.element_size() for t in (hQ1, hK1, hQ2, hK2, hg))
-    d2h = hKL.numel() * 4
+    # Every step copies its inputs from pinned host memory and reads back all it
+    # returns (KL, LSE1, LSE2 and, with the backward, dQ/dK of both settings).
+    # Inputs and outputs are double-buffered on the device: step k+1's inputs
+    # are copied in on one side stream and step k's outputs copied out on
+    # another while the kernels run.  The timed region starts before the first
+    # input copy and ends after the last output copy.
+    host_in = tuple(t.cpu().pin_memory() for t in ins)
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    in_sets = [ins, tuple(torch.empty_like(t) for t in ins)]
+    out_sets = [out, outputs()]
+    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    copied, freed = [torch.cuda.Event(), torch.cuda.Event()], [torch.cuda.Event(), torch.cuda.Event()]
+    computed, read_out = [torch.cuda.Event(), torch.cuda.Event()], [torch.cuda.Event(), torch.cuda.Event()]
 
-    # Every step copies its inputs from pinned host memory and reads its KL rows
-    # back.  The copies of step k+1 run on a side stream into a second input set
-    # while step k computes (double buffering), so they overlap the kernels; the
-    # timed region starts before the first copy and ends after the last read.
-    host = (hQ1, hK1, hQ2, hK2, hg)
-    sets = [(Q1, K1, Q2, K2, g), tuple(torch.empty_like(t) for t in (Q1, K1, Q2, K2, g))]
-    copy_stream = torch.cuda.Stream(dev)
-    copied = [torch.cuda.Event(), torch.cuda.Event()]
-    freed = [torch.cuda.Event(), torch.cuda.Event()]
-
-    def step_on(ts):
-        q1, k1, q2, k2, gg = ts
-        streamkl.kl_fwd(q1, k1, q2, k2, causal=w.causal, workspace=wsp, out=(KL, L1, L2))
-        if with_bwd:
-            for setting in (1, 2):
-                streamkl.kl_bwd(setting, gg, q1, k1, q2, k2, KL, L1, L2, causal=w.causal, workspace=wsp,
-                                out=(dQ, dK))
-
-    def issue_copy(k, after=None):
+    def issue_copy_in(k, after=None):
         slot = k % 2
-        with torch.cuda.stream(copy_stream):
+        with torch.cuda.stream(h2d_stream):
             if after is not None:
-                copy_stream.wait_event(after)
+                h2d_stream.wait_event(after)
             if k >= 2:
-                copy_stream.wait_event(freed[slot])  # step k-2 is done with this input set
-            for dst, src in zip(sets[slot], host):
+                h2d_stream.wait_event(freed[slot])  # step k-2 is done with this input set
+            for dst, src in zip(in_sets[slot], host_in):
                 dst.copy_(src, non_blocking=True)
-            copied[slot].record(copy_stream)
+            copied[slot].record(h2d_stream)
 
-    def run_e2e(n, start=None):
-        issue_copy(0, after=start)
+    def run_e2e(n, start_ev=None):
+        issue_copy_in(0, after=start_ev)
         for k in range(n):
             slot = k % 2
             stream.wait_event(copied[slot])
-            step_on(sets[slot])
+            if k >= 2:
+                stream.wait_event(read_out[slot])  # step k-2's outputs have been copied out
+            step_on(in_sets[slot], out_sets[slot])
             freed[slot].record(stream)
-            hKL.copy_(KL, non_blocking=True)
+            computed[slot].record(stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(computed[slot])
+                for key, t in out_sets[slot].items():
+                    host_out[key].copy_(t, non_blocking=True)
+                read_out[slot].record(d2h_stream)
             if k + 1 < n:
-                issue_copy(k + 1)
+                issue_copy_in(k + 1)
+        stream.wait_event(read_out[(n - 1) % 2])
 
     run_e2e(2)
     torch.cuda.synchronize()
@@ -381,27 +436,80 @@ def run_gpu(args):
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(gpu_id(dev)) as e2e_clk:
         a.record(stream)
-        run_e2e(args.steps, start=a)
+        run_e2e(args.steps, start_ev=a)
         b.record(stream)
         torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, ws_, dev)
-    e2e = {"value": step_flops * ws_ / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "clocks": e2e_clk.summary()}
-    kl_mean = float(hKL.double().mean())
+    e2e = {"value": step_flops_all / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "read_back": sorted(host_out), "clocks": e2e_clk.summary()}
+    kl_mean = float(host_out["KL"].double().mean())
+    del in_sets, out_sets, host_in, host_out, out, ins, Q1, K1, Q2, K2, g
+    torch.cuda.empty_cache()
 
-    out = None
+    decode = run_decode_leg(args, dev, rank, ws_, peaks) if not args.no_decode else None
+
+    result = None
     if rank == 0:
-        out = {
+        result = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws_, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) teacher, student +0.3 N(0,1))",
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) teacher, student +0.3 N(0,1))",
             "config": config_for(w, ws_),
             "kernels": kernels, "roofline": roofline, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "device_error_word": status, "kl_mean": kl_mean,
-            "peaks": {"bf16_tflops": peaks["bf16_tflops"], "hbm_gbs": peaks["hbm_gbs"], "source": peak_src},
+            "peaks": {"bf16_tflops": peaks["bf16_tflops"], "bf16_tflops_sustained": peak_sus,
+                      "hbm_gbs": peaks["hbm_gbs"], "source": peak_src},
         }
-        out["clocks"] = step_clocks
-    return out, w
+        if decode is not None:
+            result.update(decode_ms=decode["ms"], decode_gbs=decode["gbs"], decode_frac_hbm=decode["frac_hbm"],
+                          decode=decode)
+        result["clocks"] = step_clocks
+    return result, w
+
+
+def run_decode_leg(args, dev, rank, world, peaks):
+    """The N_Q=1 Split-K decode forward against 512K keys (B=4, H=32, d=128),
+    timed after the headline step: every key byte is read once, so HBM bounds
+    it.  Each rank takes its share of the 128 heads; GB/s counts the bytes of
+    every rank over the slowest rank's median time."""
+    from attention_kl_divergence_gb300 import streamkl
+    w = WORKLOADS[DECODE_WORKLOAD]
+    start, stop = rank_heads(w, rank, world)
+    full = make_workload(w, device=dev)
+    Q1, K1, Q2, K2 = (shard(t, start, stop).clone() for t in full)
+    del full
+    torch.cuda.empty_cache()
+    plan = streamkl.fwd_plan(Q1, K1, causal=w.causal)
+    wsp = streamkl.new_workspace(plan.workspace_bytes, dev)
+    out = tuple(torch.empty((1, Q1.shape[1], w.Nq), dtype=torch.float32, device=dev) for _ in range(3))
+    l2_flush = torch.empty(int(256e6) // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    reps = max(20, args.steps)
+    for _ in range(max(3, args.warmup)):
+        streamkl.kl_fwd(Q1, K1, Q2, K2, causal=w.causal, workspace=wsp, out=out)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    barrier(world)
+    with ClockSampler(gpu_id(dev)) as clk:
+        for a, b in ev:
+            flush_l2(l2_flush)
+            a.record(stream)
+            streamkl.kl_fwd(Q1, K1, Q2, K2, causal=w.causal, workspace=wsp, out=out)
+            b.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(statistics.median(a.elapsed_time(b) for a, b in ev), world, dev)
+    status = streamkl.workspace_status(wsp)
+    gbs = w.fwd_bytes() / ms / 1e6
+    del Q1, K1, Q2, K2, out, l2_flush
+    torch.cuda.empty_cache()
+    return {"workload": f"{w.name}: B={w.B} H={w.H} N_Q={w.Nq} N_K={w.Nk} d={w.d} non-causal, forward only",
+            "ms": ms, "gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "bytes_per_call": w.fwd_bytes(),
+            "splits": plan.num_splits, "launches_per_call": plan.launches, "reps": reps,
+            "kernel": "fwd_decode_kernel" + (" + combine_kernel" if plan.num_splits > 1 else ""),
+            "device_error_word": status, "clocks": clk.summary(), "l2": "256 MB write between calls"}
 
 
 def run_reference(args):
@@ -421,7 +529,7 @@ def run_reference(args):
     return {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": ws_, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_flops / (v * 1e12) * 1e3, "ms_per_step_kind": "extrapolated",
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded N(0,1) teacher, student +0.3 N(0,1))", "config": config_for(w, ws_),
         "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
                          "sample": last["sample"]},
@@ -497,6 +605,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="streamkl", choices=["streamkl", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
+    ap.add_argument("--no-decode", action="store_true", help="skip the N_Q=1 decode leg")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(WORKLOADS),
                     help="another named workload (the headline metric is quoted on 64k_causal)")
     ap.add_argument("--ablate", action="store_true",

@@ -130,6 +130,15 @@ STREAMKL_API streamkl_status streamkl_fwd(const streamkl_shape* shape, const voi
 STREAMKL_API streamkl_status streamkl_bwd_plan(const streamkl_shape* shape, int setting, int causal,
                                   const streamkl_options* opt, streamkl_plan* plan);
 
+/* Workspace sizes alone, with the default options (opt == NULL): the
+ * workspace_bytes field of streamkl_fwd_plan / streamkl_bwd_plan.  They return
+ * 0 when the shape, causal flag or setting is invalid or no CUDA device is
+ * current (a valid call always needs at least the 256-byte status word).
+ * Options that change the size (forced splits, bf16 gradients) need the plan
+ * queries. */
+STREAMKL_API size_t streamkl_fwd_workspace_bytes(const streamkl_shape* shape, int causal);
+STREAMKL_API size_t streamkl_bwd_workspace_bytes(const streamkl_shape* shape, int setting, int causal);
+
 /* Backward (Methodology 2).  Gradient of sum_i g[i] * KL[i] with respect to
  * the trainable side:
  *   setting 1 (teacher fixed): dQ = dL/dQ2, dK = dL/dK2, dS2 = g (P2 - P1)
@@ -162,16 +171,30 @@ STREAMKL_API streamkl_status streamkl_bwd(const streamkl_shape* shape, int setti
  * bytes that every GPU which loads the library holds until the process
  * exits.  A shape whose plan needs more scratch than that (20 bytes per
  * query row and key split, plus 256) returns STREAMKL_ERR_WORKSPACE and
- * launches nothing.  The first call on a device looks up the array's device
- * address (once per device, with that device current); make that first call
- * before any stream capture.  Each call clears the error word it uses; all
- * calls share the one array, so calls that may overlap on the GPU (different
- * streams, or different host threads) race on it and must be serialised by
- * the caller.  Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+ * launches nothing.  Every call looks up the array's device address on the
+ * current device (a table lookup, no allocation); the first call on a device
+ * also loads the library's device code there, so make that first call before
+ * any stream capture.  All calls share the one array, so calls that may
+ * overlap on the GPU (different streams, or different host threads) race on
+ * it and must be serialised by the caller.
+ *
+ * A bounded wait inside the kernels that gives up (see wait_limit_ns) does
+ * not change the return value, which only covers validation and launch: the
+ * rows that the giving-up CTA owned come back as NaN, and the scratch's
+ * device error word is set.  Read it with streamkl_noalloc_status after the
+ * call and before the next one, which clears the word when it starts.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
 STREAMKL_API streamkl_status streamkl_fwd_noalloc(const streamkl_shape* shape, const void* Q1, const void* K1,
                                                   const void* Q2, const void* K2, float scale, int causal, float* KL,
                                                   float* LSE1, float* LSE2, const streamkl_options* opt,
                                                   streamkl_stream_t stream);
+
+/* streamkl_workspace_status for the built-in scratch of streamkl_fwd_noalloc
+ * on the current device: synchronises `stream`, reads the device error word
+ * into *device_error (if not NULL), clears it, and returns
+ * STREAMKL_ERR_TIMEOUT if it was set, STREAMKL_OK otherwise (CUDA on a failed
+ * copy).  Allocates nothing. */
+STREAMKL_API streamkl_status streamkl_noalloc_status(streamkl_stream_t stream, uint32_t* device_error);
 
 /* Synchronises `stream`, reads the workspace's device error word into
  * *device_error (if not NULL), clears it, and returns STREAMKL_ERR_TIMEOUT if

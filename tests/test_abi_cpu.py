@@ -79,3 +79,12 @@ def test_options_reject_unknown_debug_flags_without_device():
     rc = lib.streamkl_fwd(ctypes.byref(_shape()), *[P(256)] * 4, ctypes.c_float(0.0), 0, *[P(256)] * 3, P(256),
                           4096, ctypes.byref(bad), P(0))
     assert rc in (sk.ERR_INVALID_ARG, sk.ERR_CUDA)  # the option check needs no device but runs in the planner
+
+
+def test_workspace_size_queries_reject_invalid_shapes_without_device():
+    lib = sk.load()
+    assert lib.streamkl_fwd_workspace_bytes(None, 0) == 0
+    assert lib.streamkl_fwd_workspace_bytes(ctypes.byref(_shape(d=96)), 0) == 0
+    assert lib.streamkl_fwd_workspace_bytes(ctypes.byref(_shape(Nq=300, Nk=200)), 1) == 0
+    assert lib.streamkl_bwd_workspace_bytes(ctypes.byref(_shape()), 3, 0) == 0  # no setting 3
+    assert lib.streamkl_bwd_workspace_bytes(ctypes.byref(_shape(B=0)), 1, 0) == 0

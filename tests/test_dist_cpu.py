@@ -69,3 +69,27 @@ def test_two_gloo_ranks_shard_heads_without_collectives():
         p.join(timeout=60)
     assert ok is True, ok
     assert mx == 1.5
+
+
+def test_bench_shards_cover_every_head_of_the_problem_once():
+    """bench.py under torchrun splits one problem's heads across the ranks
+    (strong scaling): every query and key head is owned by exactly one rank,
+    and a shard of the tensors is exactly those heads."""
+    import bench
+    from attention_kl_divergence_gb300 import WORKLOADS
+    for name in ("64k_causal", "64k_causal_gqa", "decode_q1_k512k", "512k_causal"):
+        w = WORKLOADS[name]
+        hk = w.H_kv or w.H
+        group = w.H // hk
+        for world in (1, 2, 3, 4, 8):
+            keys, queries = [], []
+            for r in range(world):
+                a, b = bench.rank_heads(w, r, world)
+                keys.extend(range(a, b))
+                queries.extend(range(a * group, b * group))
+            assert keys == list(range(w.B * hk)), (name, world)
+            assert queries == list(range(w.B * w.H)), (name, world)
+    t = torch.arange(2 * 4 * 3 * 2).reshape(2, 4, 3, 2)
+    s = bench.shard(t, 1, 3, group=2)  # key heads 1, 2 -> query heads 2..5 of the flat (b, h) order
+    assert s.shape == (1, 4, 3, 2) and s.is_contiguous()
+    assert torch.equal(s[0], t.reshape(8, 3, 2)[2:6])

@@ -7,10 +7,10 @@ Workloads (seeded synthetic inputs, see attention_kl_divergence_gb300.inputs):
   decode-shaped backward, B4 H32 N_Q=16 N_K=128K d128, both settings;
   64K causal and non-causal, B1 H32 d128; decode Split-K, B4 H32 d128,
   N_Q in {1, 16}, N_K in {128K, 512K}; 512K causal, B1 H8 d128, teacher x1.5.
-A key's dK needs every query row that sees it, so dK is sampled among the
-last keys of a causal sequence (few rows see them); non-causal 64K dK is
-checked through sum_j dK_j = 0 and fused/split agreement, with full dK parity
-on smaller non-causal shapes in test_bwd_gpu.py.
+A key's dK needs every query row that sees it: dK is sampled among the last
+keys of a causal sequence (few rows see them), and for keys spread over one
+whole head of 64K causal and 64K non-causal, where the oracle computes the
+statistics of all 65536 rows of that head once per call.
 """
 import numpy as np
 import pytest
@@ -33,6 +33,10 @@ def head(t, bh):
 def rows_for_head(Nq, n, rng):
     rows = set(rng.integers(0, Nq, size=n).tolist()) | {0, 1, 127, 128, Nq - 129, Nq - 1}
     return np.array(sorted(r for r in rows if 0 <= r < Nq), dtype=np.int64)
+
+
+KEYS_ACROSS_64K = np.array([0, 1, 127, 128, 129, 4095, 16384, 32767, 32768, 49151, 65536 - 129, 65535],
+                           dtype=np.int64)
 
 
 def check_forward(w, KL, L1, L2, inputs, heads, rows_per_head, seed):
@@ -102,11 +106,33 @@ def test_64k_causal_dk_of_keys_across_the_sequence():
     dQ, dK = streamkl.kl_bwd(1, g, *inputs, KL, L1, L2, causal=w.causal)
     torch.cuda.synchronize()
     bh = 13
-    keys = np.array([0, 1, 127, 128, 129, 4095, 16384, 32767, 32768, 49151, w.Nk - 129, w.Nk - 1], dtype=np.int64)
+    keys = KEYS_ACROSS_64K
     rk = oracle.bwd_dk_keys(1, g.reshape(-1, w.Nq)[bh][None, None], *[head(t, bh) for t in inputs], keys,
                             causal=w.causal)
     gk = dK.reshape(-1, w.Nk, w.d)[bh][torch.as_tensor(keys, device=DEV)]
     assert_grad(gk, rk, "dK of keys across a 64K causal head (setting 1)")
+
+
+def test_64k_noncausal_dk_of_keys_across_the_sequence_both_settings():
+    """dK of keys spread over one whole 64K non-causal head, first and last
+    keys included, in both settings: every key's gradient sums over all 65536
+    query rows (the longest accumulation the fused kernel keeps in tensor
+    memory, with every query tile of the head visiting the key's CTA)."""
+    w = WORKLOADS["64k"]
+    inputs = make_workload(w, device=DEV)
+    KL, L1, L2 = streamkl.kl_fwd(*inputs, causal=w.causal)
+    g = make_g(w.B, w.H, w.Nq, w.g_value, device=DEV)
+    bh = 21
+    hq = [head(t, bh) for t in inputs]
+    hg = g.reshape(-1, w.Nq)[bh][None, None]
+    keys = torch.as_tensor(KEYS_ACROSS_64K, device=DEV)
+    for setting in (1, 2):
+        dQ, dK = streamkl.kl_bwd(setting, g, *inputs, KL, L1, L2, causal=w.causal)
+        torch.cuda.synchronize()
+        gk = dK.reshape(-1, w.Nk, w.d)[bh][keys].cpu()
+        del dQ, dK
+        rk = oracle.bwd_dk_keys(setting, hg, *hq, KEYS_ACROSS_64K, causal=w.causal)
+        assert_grad(gk, rk, f"dK of keys across a 64K non-causal head (setting {setting})")
 
 
 def test_64k_noncausal_forward_and_both_settings():
@@ -164,10 +190,10 @@ def test_decode_shaped_backward_both_settings():
                  keys_per_head=32)
 
 
-def test_64k_causal_shared_keys_forward_and_setting1():
+def test_64k_causal_shared_keys_forward_and_both_settings():
     """64K causal, 32 query heads on 8 key heads: sampled rows of KL, LSE and
     dQ of query heads, and dK of the last keys of a key head, which sums the
-    gradients of its 4 query heads."""
+    gradients of its 4 query heads -- for both settings."""
     w = WORKLOADS["64k_causal_gqa"]
     inputs = make_workload(w, device=DEV)
     Q1, K1, Q2, K2 = inputs
@@ -188,18 +214,20 @@ def test_64k_causal_shared_keys_forward_and_setting1():
         assert_lse(L2[0, h][idx], rL2, f"LSE2 head {h}")
         assert_kl(KL[0, h][idx], rKL, f"KL head {h}")
     g = make_g(w.B, w.H, w.Nq, w.g_value, device=DEV)
-    dQ, dK = streamkl.kl_bwd(1, g, *inputs, KL, L1, L2, causal=w.causal)
-    torch.cuda.synchronize()
-    assert dK.shape[1] == w.H_kv
-    gq, rq = [], []
-    for h in (0, 13, 31):
-        rows = rows_for_head(w.Nq, 16, rng)
-        rq.append(oracle.bwd_dq_rows(1, g[0, h][None, None], *views(h), rows, causal=w.causal))
-        gq.append(dQ[0, h][torch.as_tensor(rows, device=DEV)])
-    assert_grad(torch.cat(gq), np.concatenate(rq), "dQ rows, shared keys (setting 1)")
-    hk = 3
-    keys = np.array(sorted(set(rng.integers(w.Nk - 512, w.Nk, size=16).tolist()) | {w.Nk - 512, w.Nk - 1}),
-                    dtype=np.int64)
-    rk = sum(oracle.bwd_dk_keys(1, g[0, h][None, None], *views(h), keys, causal=w.causal)
-             for h in range(hk * group, (hk + 1) * group))
-    assert_grad(dK[0, hk][torch.as_tensor(keys, device=DEV)], rk, "dK keys of a shared key head (setting 1)")
+    for setting, hk in ((1, 3), (2, 6)):
+        dQ, dK = streamkl.kl_bwd(setting, g, *inputs, KL, L1, L2, causal=w.causal)
+        torch.cuda.synchronize()
+        assert dK.shape[1] == w.H_kv
+        gq, rq = [], []
+        for h in (0, 13, 31):
+            rows = rows_for_head(w.Nq, 16, rng)
+            rq.append(oracle.bwd_dq_rows(setting, g[0, h][None, None], *views(h), rows, causal=w.causal))
+            gq.append(dQ[0, h][torch.as_tensor(rows, device=DEV)])
+        assert_grad(torch.cat(gq), np.concatenate(rq), f"dQ rows, shared keys (setting {setting})")
+        keys = np.array(sorted(set(rng.integers(w.Nk - 512, w.Nk, size=16).tolist()) | {w.Nk - 512, w.Nk - 1}),
+                        dtype=np.int64)
+        rk = sum(oracle.bwd_dk_keys(setting, g[0, h][None, None], *views(h), keys, causal=w.causal)
+                 for h in range(hk * group, (hk + 1) * group))
+        assert_grad(dK[0, hk][torch.as_tensor(keys, device=DEV)], rk,
+                    f"dK keys of a shared key head (setting {setting})")
+        del dQ, dK
