@@ -463,6 +463,93 @@ streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const flo
     return STREAMKL_OK;
 }
 
+streamkl_status streamkl_bwd_joint_plan(const streamkl_shape* shape, int causal, const streamkl_options* opt,
+                                        streamkl_plan* plan) {
+    if (!plan) return STREAMKL_ERR_INVALID_ARG;
+    streamkl_status st = check_shape(shape, causal);
+    if (st != STREAMKL_OK) return st;
+    if (opt && (opt->bwd_mode != 0 || (opt->grad_bf16 != 0 && opt->grad_bf16 != 1) ||
+                (opt->debug_flags & ~STREAMKL_DEBUG_INJECT_STALL)))
+        return STREAMKL_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return STREAMKL_ERR_CUDA;
+    const int64_t ctas_kv = int64_t(shape->B) * kv_heads(shape) * ((shape->Nk + kBlockK - 1) / kBlockK);
+    const int64_t ctas_q = int64_t(shape->B) * shape->H * ((shape->Nq + kBlockQ - 1) / kBlockQ);
+    if (ctas_kv > INT32_MAX || ctas_q > INT32_MAX) return STREAMKL_ERR_UNSUPPORTED;
+    plan->path = 5;
+    plan->num_splits = 1;
+    plan->num_ctas = static_cast<int>(ctas_kv);
+    plan->launches = 2;
+    plan->workspace_bytes = kStatusBytes;
+    return STREAMKL_OK;
+}
+
+streamkl_status streamkl_bwd_joint(const streamkl_shape* shape, const float* g, const void* Q1, const void* K1,
+                                   const void* Q2, const void* K2, const float* KL, const float* LSE1,
+                                   const float* LSE2, float scale, int causal, void* dQ1, void* dK1, void* dQ2,
+                                   void* dK2, void* workspace, size_t workspace_bytes, const streamkl_options* opt,
+                                   streamkl_stream_t stream) {
+    streamkl_status st = check_shape(shape, causal);
+    if (st != STREAMKL_OK) return st;
+    const void* qk[4] = {Q1, K1, Q2, K2};
+    for (const void* q : qk)
+        if (!q || !aligned16(q)) return STREAMKL_ERR_INVALID_ARG;
+    const void* rows[4] = {g, KL, LSE1, LSE2};
+    for (const void* q : rows)
+        if (!q || (reinterpret_cast<uintptr_t>(q) & 3u) != 0) return STREAMKL_ERR_INVALID_ARG;
+    const void* grads[4] = {dQ1, dK1, dQ2, dK2};
+    for (const void* q : grads)
+        if (!q || !aligned16(q)) return STREAMKL_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace)) return STREAMKL_ERR_WORKSPACE;
+    streamkl_plan plan{};
+    if ((st = streamkl_bwd_joint_plan(shape, causal, opt, &plan)) != STREAMKL_OK) return st;
+    if (workspace_bytes < plan.workspace_bytes) return STREAMKL_ERR_WORKSPACE;
+
+    const float sc = resolve_scale(scale, shape->d);
+    BwdParams p{};
+    p.B = shape->B;
+    p.H = shape->H;
+    p.Nq = shape->Nq;
+    p.Nk = shape->Nk;
+    p.causal = causal ? 1 : 0;
+    p.diag_off = shape->Nk - shape->Nq;
+    p.H_kv = kv_heads(shape);
+    p.kv_group = shape->H / p.H_kv;
+    p.scale = sc;
+    p.scale_log2e = sc * 1.4426950408889634f;
+    p.g = g;
+    p.KL = KL;
+    p.LSE1 = LSE1;
+    p.LSE2 = LSE2;
+    p.dQ = dQ1;
+    p.dK = dK1;
+    p.dQb = dQ2;
+    p.dKb = dK2;
+    p.grad_bf16 = (opt && opt->grad_bf16 == 1) ? 1 : 0;
+    p.dQacc = nullptr;
+    p.status = static_cast<unsigned int*>(workspace);
+    p.wait_ns = static_cast<unsigned long long>(wait_limit(opt));
+    p.inject_stall = (opt && (opt->debug_flags & STREAMKL_DEBUG_INJECT_STALL)) ? 1 : 0;
+
+    // query-tile kernel: Q boxes of 128 rows, K boxes of 64 rows; key-tile kernel: the reverse
+    CUtensorMap qm[4], kv[4];
+    if (!make_map(&qm[0], Q1, shape, true, kBlockQ) || !make_map(&qm[1], K1, shape, false, 64) ||
+        !make_map(&qm[2], Q2, shape, true, kBlockQ) || !make_map(&qm[3], K2, shape, false, 64) ||
+        !make_map(&kv[0], Q1, shape, true, 64) || !make_map(&kv[1], K1, shape, false, kBlockK) ||
+        !make_map(&kv[2], Q2, shape, true, 64) || !make_map(&kv[3], K2, shape, false, kBlockK))
+        return STREAMKL_ERR_CUDA;
+    BwdParams pq = p, pkv = p;
+    pq.num_q_tiles = (shape->Nq + kBlockQ - 1) / kBlockQ;
+    pq.num_k_tiles = (shape->Nk + 63) / 64;
+    pkv.num_q_tiles = (shape->Nq + 63) / 64;
+    pkv.num_k_tiles = (shape->Nk + kBlockK - 1) / kBlockK;
+    const int ctas_q = static_cast<int>(int64_t(shape->B) * shape->H * pq.num_q_tiles);
+    if (launch_bwd_joint(shape->d, qm, kv, pq, pkv, ctas_q, plan.num_ctas, reinterpret_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return STREAMKL_ERR_CUDA;
+    return STREAMKL_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

@@ -74,6 +74,38 @@ __device__ __forceinline__ void row_constants(const BwdParams& p, size_t row, bo
     g = p.g[row];
 }
 
+// Per-row constants of the joint recompute (both settings at once):
+//   la = LSE1 * log2(e), lb = LSE2 * log2(e), xb = LSE1 - LSE2 + KL, g.
+__device__ __forceinline__ void row_constants_joint(const BwdParams& p, size_t row, bool valid, float& la,
+                                                    float& lb, float& xb, float& g) {
+    constexpr float kLog2e = 1.4426950408889634f;
+    if (!valid) {
+        la = lb = xb = g = 0.f;
+        return;
+    }
+    const float l1 = p.LSE1[row], l2 = p.LSE2[row];
+    la = l1 * kLog2e;
+    lb = l2 * kLog2e;
+    xb = (l1 - l2) + p.KL[row];
+    g = p.g[row];
+}
+
+// dS of both settings for two pairs from one recompute, FP32x2:
+//   d1 = g s P1 (s (z1 - z2) - xb)   setting 2: gradients to the teacher
+//   d2 = g s (P2 - P1)               setting 1: gradients to the student
+// with nla = -la, nlb = -lb, nxb = -xb, gs = g * scale.
+__device__ __forceinline__ void dscore_joint2(float2 z1, float2 z2, float2 cc, float2 sc, float2 nla, float2 nlb,
+                                              float2 nxb, float2 gs, float2& d1, float2& d2) {
+    const float2 neg = make_float2(-1.f, -1.f);
+    const float2 x1 = __ffma2_rn(z1, cc, nla);
+    const float2 x2 = __ffma2_rn(z2, cc, nlb);
+    const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+    const float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+    d2 = __fmul2_rn(gs, __ffma2_rn(p1, neg, p2));
+    const float2 df = __ffma2_rn(z2, neg, z1);
+    d1 = __fmul2_rn(__fmul2_rn(gs, p1), __ffma2_rn(df, sc, nxb));
+}
+
 // Write 32 dS values as two bf16 terms, hi = bf16(v) and lo = bf16(v - hi),
 // each as four 16-byte chunks of a 128-byte swizzled row of its own tile.
 // The gradient GEMMs consume hi and lo with the same other operand, so dS

@@ -59,8 +59,10 @@ struct BwdParams {
     const float* KL;
     const float* LSE1;
     const float* LSE2;
-    void* dQ;            // [B*H*Nq, d] float32 or bf16 (grad_bf16)
-    void* dK;            // [B*H_kv*Nk, d] float32 or bf16
+    void* dQ;            // [B*H*Nq, d] float32 or bf16 (grad_bf16); joint backward: the teacher's dQ1
+    void* dK;            // [B*H_kv*Nk, d] float32 or bf16; joint backward: the teacher's dK1
+    void* dQb;           // joint backward only: the student's dQ2, laid out like dQ
+    void* dKb;           // joint backward only: the student's dK2, laid out like dK
     float* dQacc;        // fused mode: float32 [B*H*Nq, d] the dQ tiles are added into
     int grad_bf16;
     unsigned int* status;

@@ -23,6 +23,11 @@ cudaError_t launch_bwd_kv(int d, int setting, bool fused, const CUtensorMap* map
                           cudaStream_t stream);
 // Key-split backward for at most 16 query rows per key head: Q maps with boxes
 // of Nq rows x kv_group heads, K maps with 128-row boxes; p.num_splits set.
+// Joint backward (both sides from one recompute of the scores per kernel):
+// qmaps as for bwd_q, kvmaps as for bwd_kv; p.dQ/p.dK take the teacher's
+// gradients, p.dQb/p.dKb the student's.
+cudaError_t launch_bwd_joint(int d, const CUtensorMap* qmaps, const CUtensorMap* kvmaps, const BwdParams& pq,
+                             const BwdParams& pkv, int ctas_q, int ctas_kv, cudaStream_t stream);
 cudaError_t launch_bwd_decode(int d, int setting, const CUtensorMap* maps, const BwdParams& p, int ctas,
                               cudaStream_t stream);
 

@@ -22,7 +22,7 @@ import torch
 from . import build as _build
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
-PATH_TILE, PATH_DECODE, PATH_BWD_FUSED, PATH_BWD_SPLIT, PATH_BWD_KEYSPLIT = range(5)
+PATH_TILE, PATH_DECODE, PATH_BWD_FUSED, PATH_BWD_SPLIT, PATH_BWD_KEYSPLIT, PATH_BWD_JOINT = range(6)
 BWD_AUTO, BWD_FUSED, BWD_SPLIT, BWD_KEYSPLIT = 0, 1, 2, 3
 
 
@@ -54,7 +54,8 @@ class StreamKLError(RuntimeError):
 
 EXPORTED = ("streamkl_fwd_plan", "streamkl_fwd", "streamkl_bwd_plan", "streamkl_bwd", "streamkl_workspace_status",
             "streamkl_status_string", "streamkl_version", "streamkl_fwd_noalloc", "streamkl_noalloc_status",
-            "streamkl_fwd_workspace_bytes", "streamkl_bwd_workspace_bytes")
+            "streamkl_fwd_workspace_bytes", "streamkl_bwd_workspace_bytes", "streamkl_bwd_joint_plan",
+            "streamkl_bwd_joint")
 
 _lock = threading.Lock()
 _lib = None
@@ -84,6 +85,8 @@ def load(build_if_stale: bool = True):
         lib.streamkl_workspace_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
         lib.streamkl_fwd_noalloc.argtypes = [sp, P, P, P, P, F, I, P, P, P, op, P]
         lib.streamkl_noalloc_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+        lib.streamkl_bwd_joint_plan.argtypes = [sp, I, op, pp]
+        lib.streamkl_bwd_joint.argtypes = [sp, P, P, P, P, P, P, P, P, F, I, P, P, P, P, P, Z, op, P]
         lib.streamkl_fwd_workspace_bytes.argtypes = [sp, I]
         lib.streamkl_bwd_workspace_bytes.argtypes = [sp, I, I]
         lib.streamkl_fwd_workspace_bytes.restype = Z
@@ -92,7 +95,7 @@ def load(build_if_stale: bool = True):
         lib.streamkl_status_string.restype = ctypes.c_char_p
         for name in ("streamkl_fwd_plan", "streamkl_fwd", "streamkl_bwd_plan", "streamkl_bwd",
                      "streamkl_workspace_status", "streamkl_version", "streamkl_fwd_noalloc",
-                     "streamkl_noalloc_status"):
+                     "streamkl_noalloc_status", "streamkl_bwd_joint_plan", "streamkl_bwd_joint"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -274,6 +277,46 @@ def kl_bwd(setting, g, Q1, K1, Q2, K2, KL, LSE1, LSE2, causal=False, scale=None,
                           ctypes.byref(opts), _stream(Q1.device))
     _raise(rc, "streamkl_bwd")
     return dQ, dK
+
+
+def bwd_joint_plan(Q1, K1, causal=False, grad_dtype=torch.float32) -> Plan:
+    plan = Plan()
+    _raise(load().streamkl_bwd_joint_plan(ctypes.byref(make_shape(Q1, K1)), int(bool(causal)),
+                                          ctypes.byref(_opts(grad_bf16=_grad_flag(grad_dtype))), ctypes.byref(plan)),
+           "streamkl_bwd_joint_plan")
+    return plan
+
+
+def kl_bwd_joint(g, Q1, K1, Q2, K2, KL, LSE1, LSE2, causal=False, scale=None, workspace=None, out=None,
+                 wait_limit_ns=0, debug_flags=0, grad_dtype=torch.float32):
+    """(dQ1, dK1, dQ2, dK2): the gradients of both sides from one recompute of
+    the scores per kernel -- the teacher's as in setting 2, the student's as
+    in setting 1 (streamkl_bwd_joint)."""
+    _check_qk(Q1, K1, Q2, K2)
+    lib = load()
+    shape = make_shape(Q1, K1)
+    opts = _opts(0, 0, wait_limit_ns, debug_flags, _grad_flag(grad_dtype))
+    plan = Plan()
+    _raise(lib.streamkl_bwd_joint_plan(ctypes.byref(shape), int(bool(causal)), ctypes.byref(opts),
+                                       ctypes.byref(plan)), "streamkl_bwd_joint_plan")
+    B, H, Nq, d = Q1.shape
+    Hk, Nk = K1.shape[1], K1.shape[2]
+    for name, t in (("g", g), ("KL", KL), ("LSE1", LSE1), ("LSE2", LSE2)):
+        _check_tensor(name, t, (B, H, Nq), torch.float32, Q1.device)
+    if out is None:
+        out = tuple(torch.empty(shp, dtype=grad_dtype, device=Q1.device)
+                    for shp in ((B, H, Nq, d), (B, Hk, Nk, d), (B, H, Nq, d), (B, Hk, Nk, d)))
+    for name, t, shp in zip(("dQ1", "dK1", "dQ2", "dK2"), out,
+                            ((B, H, Nq, d), (B, Hk, Nk, d), (B, H, Nq, d), (B, Hk, Nk, d))):
+        _check_tensor(name, t, shp, grad_dtype, Q1.device)
+    workspace = _check_workspace(workspace, plan.workspace_bytes, Q1.device)
+    dQ1, dK1, dQ2, dK2 = out
+    rc = lib.streamkl_bwd_joint(ctypes.byref(shape), _ptr(g), _ptr(Q1), _ptr(K1), _ptr(Q2), _ptr(K2), _ptr(KL),
+                                _ptr(LSE1), _ptr(LSE2), ctypes.c_float(0.0 if scale is None else float(scale)),
+                                int(bool(causal)), _ptr(dQ1), _ptr(dK1), _ptr(dQ2), _ptr(dK2), _ptr(workspace),
+                                workspace.numel(), ctypes.byref(opts), _stream(Q1.device))
+    _raise(rc, "streamkl_bwd_joint")
+    return dQ1, dK1, dQ2, dK2
 
 
 def workspace_status(workspace) -> int:

@@ -383,6 +383,36 @@ def run_gpu(args):
                     "share_of_step": kernels[top]["ms"] / step_ms, "flops_per_launch": flops_top,
                     "peak_source": f"bf16_tflops ({peak_src}, burst)"}
 
+    # ---------------- joint backward: both sides from one recompute per kernel,
+    # timed on its own against the two single-setting passes of the step
+    joint = None
+    if with_bwd and not args.no_joint:
+        jplan = streamkl.bwd_joint_plan(Q1, K1, causal=w.causal)
+        jout = (out["dQ1"], out["dK1"], out["dQ2"], out["dK2"])
+
+        def joint_call():
+            streamkl.kl_bwd_joint(g, Q1, K1, Q2, K2, out["KL"], out["LSE1"], out["LSE2"], causal=w.causal,
+                                  workspace=wsp, out=jout)
+
+        for _ in range(2):
+            joint_call()
+        jt = []
+        for _ in range(max(3, args.steps // 2)):
+            flush_l2(l2_flush)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            joint_call()
+            b.record(stream)
+            torch.cuda.synchronize()
+            jt.append(a.elapsed_time(b))
+        jms = max_over_ranks(statistics.median(jt), ws_, dev)
+        joint = {"ms": jms, "two_single_setting_passes_ms": b1_ms + b2_ms,
+                 "tflops_12d": 12 * d * pairs / jms / 1e9, "frac_bf16_peak_12d": 12 * d * pairs / jms / 1e9 / peak_tf,
+                 "kernels": "bwd_q_joint_kernel + bwd_kv_joint_kernel", "launches": jplan.launches,
+                 "note": "12*d flops per visible pair: one recompute (4d) and four gradient GEMMs (8d)"}
+        if streamkl.workspace_status(wsp):
+            raise RuntimeError("device error word set by the joint backward")
+
     # ---------------- end to end through the C ABI with host buffers
     # Every step copies its inputs from pinned host memory and reads back all it
     # returns (KL, LSE1, LSE2 and, with the backward, dQ/dK of both settings).
@@ -462,6 +492,8 @@ def run_gpu(args):
             "peaks": {"bf16_tflops": peaks["bf16_tflops"], "bf16_tflops_sustained": peak_sus,
                       "hbm_gbs": peaks["hbm_gbs"], "source": peak_src},
         }
+        if joint is not None:
+            result["bwd_joint"] = joint
         if decode is not None:
             result.update(decode_ms=decode["ms"], decode_gbs=decode["gbs"], decode_frac_hbm=decode["frac_hbm"],
                           decode=decode)
@@ -588,6 +620,12 @@ def run_ablations(args):
         KL, L1, L2 = streamkl.kl_fwd(Q1, K1, Q2, K2, causal=w.causal)
         grads = (torch.empty_like(Q1, dtype=torch.float32), torch.empty_like(K1, dtype=torch.float32))
         reps = 3 if w.Nq >= 65536 else max(args.steps, 5)
+        if "fused" in names and w.Nq > 16:
+            jo = tuple(torch.empty_like(t, dtype=torch.float32) for t in (Q1, K1, Q2, K2))
+            ms = timed(lambda: streamkl.kl_bwd_joint(g, Q1, K1, Q2, K2, KL, L1, L2, causal=w.causal, out=jo), reps)
+            emit(what="backward mode", workload=name, setting="both", mode="joint", ms=ms,
+                 tflops_12d=12 * w.d * w.visible_pairs() * w.B * w.H / ms / 1e9)
+            del jo
         for setting in (1, 2):
             for mname in names:
                 ms = timed(lambda: streamkl.kl_bwd(setting, g, Q1, K1, Q2, K2, KL, L1, L2, causal=w.causal,
@@ -606,6 +644,7 @@ def main():
     ap.add_argument("--impl", default="streamkl", choices=["streamkl", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-decode", action="store_true", help="skip the N_Q=1 decode leg")
+    ap.add_argument("--no-joint", action="store_true", help="skip timing the joint backward")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(WORKLOADS),
                     help="another named workload (the headline metric is quoted on 64k_causal)")
     ap.add_argument("--ablate", action="store_true",

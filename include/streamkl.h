@@ -103,7 +103,8 @@ typedef struct {
     int32_t path;       /* 0 = tile forward, 1 = decode (Nq <= 16, causal or not) forward,
                            2 = fused backward, 3 = separate-kernel backward,
                            4 = key-split backward (at most 16 query rows per key head;
-                               the automatic choice there) */
+                               the automatic choice there),
+                           5 = joint backward (both sides, streamkl_bwd_joint) */
     int32_t num_splits; /* key splits of the forward (1 = no combine step) or of the
                            key-split backward */
     int32_t num_ctas;   /* CTAs of the main kernel                          */
@@ -129,6 +130,30 @@ STREAMKL_API streamkl_status streamkl_fwd(const streamkl_shape* shape, const voi
 /* Plan of streamkl_bwd (fused vs separate kernels, workspace). */
 STREAMKL_API streamkl_status streamkl_bwd_plan(const streamkl_shape* shape, int setting, int causal,
                                   const streamkl_options* opt, streamkl_plan* plan);
+
+/* Joint backward (Methodology 2, both settings at once): the gradient of
+ * sum_i g[i] * KL[i] with respect to all four inputs, where the teacher's
+ * gradients differentiate through P1 with P2 held fixed (setting 2) and the
+ * student's through P2 with P1 held fixed (setting 1):
+ *   dQ1 = scale * dS1 K1,  dK1 = scale * dS1^T Q1,  dS1 = g P1 ((S1 - LSE1) - (S2 - LSE2) - KL)
+ *   dQ2 = scale * dS2 K2,  dK2 = scale * dS2^T Q2,  dS2 = g (P2 - P1)
+ * Results equal streamkl_bwd with setting 2 (dQ1, dK1) and setting 1 (dQ2,
+ * dK2), but the scores are regenerated once per kernel for both: a query-tile
+ * kernel accumulates dQ1 and dQ2, a key-tile kernel dK1 and dK2, each output
+ * written once (no atomics: the results are deterministic).  Layouts, dtypes
+ * (opt->grad_bf16) and shared keys as for streamkl_bwd; dQ1/dQ2 are
+ * [B, H, Nq, d], dK1/dK2 [B, H_kv, Nk, d].  opt->bwd_mode must be 0 and
+ * num_splits is ignored.  The workspace holds the 256-byte error word only
+ * (streamkl_bwd_joint_plan: path 5, 2 launches).
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+STREAMKL_API streamkl_status streamkl_bwd_joint_plan(const streamkl_shape* shape, int causal,
+                                                     const streamkl_options* opt, streamkl_plan* plan);
+STREAMKL_API streamkl_status streamkl_bwd_joint(const streamkl_shape* shape, const float* g, const void* Q1,
+                                                const void* K1, const void* Q2, const void* K2, const float* KL,
+                                                const float* LSE1, const float* LSE2, float scale, int causal,
+                                                void* dQ1, void* dK1, void* dQ2, void* dK2, void* workspace,
+                                                size_t workspace_bytes, const streamkl_options* opt,
+                                                streamkl_stream_t stream);
 
 /* Workspace sizes alone, with the default options (opt == NULL): the
  * workspace_bytes field of streamkl_fwd_plan / streamkl_bwd_plan.  They return
