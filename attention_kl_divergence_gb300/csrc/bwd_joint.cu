@@ -10,7 +10,8 @@
 // each kernel here recomputes S1, S2 once and forms both:
 //
 //   bwd_q_joint_kernel   one 128-row query tile; loops over 64-key tiles;
-//                        dQ1 = scale dS1 K1 and dQ2 = scale dS2 K2 in TMEM.
+//                        dQ1 = scale dS1 K1 and dQ2 = scale dS2 K2 in TMEM,
+//                        the query tiles in TMEM as the score MMAs' A operand.
 //   bwd_kv_joint_kernel  one 128-key tile; loops over 64-row query tiles;
 //                        dK1 = scale dS1^T Q1 and dK2 = scale dS2^T Q2 in TMEM.
 //
@@ -28,35 +29,46 @@ namespace {
 
 // ---------------------------------------------------------------------------
 // bwd_q_joint: CTA = 128 query rows; 64-key tiles (K1 and K2) through a ring.
-// Warps: 0 TMA, 1 TMEM + MMA, 2-9 recompute/dS (two warpgroups, one query row
-// per thread, each taking 32 of the tile's 64 keys).
-// TMEM: S1|S2 double buffered (cols 0-255), dQ1 (256-383), dQ2 (384-511).
+// Warps: 0 TMA, 1 TMEM + score MMAs, 2-9 recompute/dS (two warpgroups, one
+// query row per thread, each taking 32 of the tile's 64 keys), 10 dQ MMAs.
+// TMEM: Q1|Q2 as the A operand of the score MMAs (cols 0-127, copied in
+// once), S1|S2 (128-255, released as soon as the update warps hold it in
+// registers), dQ1 (256-383), dQ2 (384-511).
+// Two dS buffers of four tiles each (dS1 hi, lo; dS2 hi, lo); at d = 128 the
+// first takes the query tiles' shared memory, free once they are in TMEM.
 // ---------------------------------------------------------------------------
 template <int D, int NST>
 struct QJointSmem {
     static constexpr int kQBytes = kBlockQ * D * 2;    // 128 rows
     static constexpr int kKBytes = kBwdTile * D * 2;   // 64 keys
     static constexpr int kDsBytes = kBlockQ * kBwdTile * 2;
+    static constexpr int kDsBuf = 4 * kDsBytes;
+    static constexpr bool kOverlay = 2 * kQBytes >= kDsBuf;
     static constexpr int q1 = 0;
     static constexpr int q2 = kQBytes;
-    static constexpr int k = 2 * kQBytes;              // stage s: K1 at k + 2*s*kKBytes, K2 right after
-    static constexpr int ds = k + 2 * NST * kKBytes;   // dS1 hi, dS1 lo, dS2 hi, dS2 lo
-    static constexpr int bars = ds + 4 * kDsBytes;
+    static constexpr int ds0 = kOverlay ? 0 : 2 * kQBytes;
+    static constexpr int ds1 = kOverlay ? 2 * kQBytes : ds0 + kDsBuf;
+    static constexpr int k = ds1 + kDsBuf;             // stage s: K1 at k + 2*s*kKBytes, K2 right after
+    static constexpr int bars = k + 2 * NST * kKBytes;
     static constexpr int bar_q = bars;
     static constexpr int bar_kfull = bar_q + 8;
     static constexpr int bar_kempty = bar_kfull + 8 * NST;
-    static constexpr int bar_sfull = bar_kempty + 8 * NST;  // [2]
-    static constexpr int bar_sempty = bar_sfull + 16;        // [2]
-    static constexpr int bar_dsfull = bar_sempty + 16;
-    static constexpr int bar_dsempty = bar_dsfull + 8;
-    static constexpr int bar_done = bar_dsempty + 8;
-    static constexpr int misc = bar_done + 8;  // tmem base (4 B), abort flag (4 B)
+    static constexpr int bar_sfull = bar_kempty + 8 * NST;
+    static constexpr int bar_sempty = bar_sfull + 8;
+    static constexpr int bar_dsfull = bar_sempty + 8;    // [2]
+    static constexpr int bar_dsempty = bar_dsfull + 16;  // [2]
+    static constexpr int bar_done = bar_dsempty + 16;
+    static constexpr int bar_drain = bar_done + 8;  // the score issuer's own drain on abort
+    static constexpr int misc = bar_drain + 8;  // tmem base (4 B), abort flag (4 B)
     static constexpr int total = misc + 16;
     static constexpr int alloc = total + 1024;  // slack for 1024-byte alignment
 };
 
+// warp 0 TMA, warp 1 score MMAs (and TMEM), 8 update warps, the dQ-MMA warp last
+constexpr int kQJointThreads = 352;
+
 template <int D, int NST>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(kQJointThreads, 1)
     bwd_q_joint_kernel(const __grid_constant__ CUtensorMap tQ1, const __grid_constant__ CUtensorMap tK1,
                        const __grid_constant__ CUtensorMap tQ2, const __grid_constant__ CUtensorMap tK2,
                        const BwdParams p) {
@@ -84,13 +96,14 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(base + L::bar_kfull + 8 * s, 1);
             mbar_init(base + L::bar_kempty + 8 * s, 1);
         }
+        mbar_init(base + L::bar_sfull, 1);
+        mbar_init(base + L::bar_sempty, 256);
         for (int s = 0; s < 2; ++s) {
-            mbar_init(base + L::bar_sfull + 8 * s, 1);
-            mbar_init(base + L::bar_sempty + 8 * s, 256);
+            mbar_init(base + L::bar_dsfull + 8 * s, 256);
+            mbar_init(base + L::bar_dsempty + 8 * s, 1);
         }
-        mbar_init(base + L::bar_dsfull, 256);
-        mbar_init(base + L::bar_dsempty, 1);
         mbar_init(base + L::bar_done, 1);
+        mbar_init(base + L::bar_drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -136,81 +149,109 @@ __global__ void __launch_bounds__(320, 1)
             }
         }
     } else if (warp == 1) {
+        // ------------------------------------------------ score MMAs
+        // Two threads issue the MMAs: this one the scores of tile it, the last
+        // warp's first thread the dQ MMAs of earlier tiles, so that a wait or
+        // commit in one leaves the tensor pipe to the other's queued work.
         if (lane == 0) {
             constexpr uint32_t id_s = idesc_bf16_f32(kBlockQ, kBwdTile);
-            constexpr uint32_t id_dq = idesc_bf16_f32(kBlockQ, D, 0, 1);
-            const uint32_t t_dq1 = tmem + 256, t_dq2 = tmem + 384;
-            int issued = 0;
+            const uint32_t t_q = tmem, t_s = tmem + 128;
             bool started = false;
             const uint32_t dhi = smem_desc_hi();
             constexpr uint32_t kStageLo = (2 * L::kKBytes) >> 4, kK2Lo = L::kKBytes >> 4;
-            const uint32_t q1_lo = smem_desc_lo_k128(base + L::q1), q2_lo = smem_desc_lo_k128(base + L::q2);
             const uint32_t k_lo0 = smem_desc_lo_k128(base + L::k);
-            // B of dQ_t = K_t, MN-major: K1 at the stage, K2 right after it
-            const uint32_t k1mn_lo0 = smem_desc_lo_mn128(base + L::k, kBwdTile * 128);
-            const uint32_t ds_lo = smem_desc_lo_k128(base + L::ds);
-            auto issue_s = [&](int buf, uint32_t k_lo) {
-                const uint32_t d1 = tmem + buf * 128, d2 = d1 + 64;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t qo = ((kk >> 2) * kBlockQ * 128 + (kk & 3) * 32) >> 4;
-                    const uint32_t ko = ((kk >> 2) * kBwdTile * 128 + (kk & 3) * 32) >> 4;
-                    tc_mma_bf16_w(d1, q1_lo + qo, dhi, k_lo + ko, dhi, id_s, kk > 0);
-                }
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t qo = ((kk >> 2) * kBlockQ * 128 + (kk & 3) * 32) >> 4;
-                    const uint32_t ko = ((kk >> 2) * kBwdTile * 128 + (kk & 3) * 32) >> 4;
-                    tc_mma_bf16_w(d2, q2_lo + qo, dhi, k_lo + kK2Lo + ko, dhi, id_s, kk > 0);
-                }
-                tc_commit(base + L::bar_sfull + 8 * buf);
-            };
             // test aid: a wait on a barrier that nothing arrives on before the end
             const bool stalled = p.inject_stall && blockIdx.x == 0 &&
                                  !mbar_wait(base + L::bar_done, 0, wc, kErrWaitOther);
-            bool ok = !stalled && mbar_wait(base + L::bar_q, 0, wc, kErrWaitQ) &&
-                      mbar_wait(base + L::bar_kfull, 0, wc, kErrWaitK);
-            if (ok) {
+            if (!stalled && n_tiles > 0 && mbar_wait(base + L::bar_q, 0, wc, kErrWaitQ)) {
                 tc_fence_after();
-                issue_s(0, k_lo0);
-                started = true;
-                int sn = NST > 1 ? 1 : 0, s = 0;  // stages of tiles it + 1 and it
-                uint32_t pn = NST > 1 ? 0 : 1;    // phase of tile it + 1's stage
-                for (int it = 0; it < n_tiles; ++it) {
-                    if (it + 1 < n_tiles) {
-                        const int n1 = it + 1;
-                        if (!mbar_wait(base + L::bar_kfull + 8 * sn, pn, wc, kErrWaitK)) break;
-                        if (!mbar_wait(base + L::bar_sempty + 8 * (n1 & 1), ((n1 >> 1) & 1) ^ 1, wc, kErrWaitS))
-                            break;
-                        tc_fence_after();
-                        issue_s(n1 & 1, k_lo0 + sn * kStageLo);
-                        if (++sn == NST) sn = 0, pn ^= 1;
-                    }
-                    if (!mbar_wait(base + L::bar_dsfull, it & 1, wc, kErrWaitOther)) break;
-                    tc_fence_after();
-                    const uint32_t k1mn_lo = k1mn_lo0 + s * kStageLo;
-                    // dQ1 += dS1 K1 and dQ2 += dS2 K2; each dS = hi + lo
+                // the CTA's query tiles become the A operand of every score MMA; the
+                // commit after the first score tile also covers these copies, so
+                // once that tile is complete their shared memory may be reused
 #pragma unroll
-                    for (int part = 0; part < 2; ++part)
-#pragma unroll
-                        for (int kk = 0; kk < kBwdTile / 16; ++kk)
-                            tc_mma_bf16_w(t_dq1, ds_lo + ((part * L::kDsBytes + kk * 32) >> 4), dhi,
-                                          k1mn_lo + ((kk * 16 * 128) >> 4), dhi, id_dq, (it | kk | part) != 0);
-#pragma unroll
-                    for (int part = 0; part < 2; ++part)
-#pragma unroll
-                        for (int kk = 0; kk < kBwdTile / 16; ++kk)
-                            tc_mma_bf16_w(t_dq2, ds_lo + (((2 + part) * L::kDsBytes + kk * 32) >> 4), dhi,
-                                          k1mn_lo + kK2Lo + ((kk * 16 * 128) >> 4), dhi, id_dq,
-                                          (it | kk | part) != 0);
-                    tc_commit(base + L::bar_dsempty);
-                    tc_commit(base + L::bar_kempty + 8 * s);
-                    if (++s == NST) s = 0;
-                    ++issued;
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qo = (kk >> 2) * kBlockQ * 128 + (kk & 3) * 32;
+                    tc_cp_128x256b(t_q + kk * 8, smem_desc_k128(base + L::q1 + qo));
+                    tc_cp_128x256b(t_q + D / 2 + kk * 8, smem_desc_k128(base + L::q2 + qo));
                 }
-                if (issued == n_tiles) tc_commit(base + L::bar_done);
+                started = true;
+                int s = 0;
+                uint32_t ph = 0, k_lo = k_lo0;
+                for (int it = 0; it < n_tiles; ++it) {
+                    if (!mbar_wait(base + L::bar_kfull + 8 * s, ph, wc, kErrWaitK)) break;
+                    // tile it - 1's scores are in the update warps' registers
+                    if (!mbar_wait(base + L::bar_sempty, (it & 1) ^ 1, wc, kErrWaitS)) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ko = ((kk >> 2) * kBwdTile * 128 + (kk & 3) * 32) >> 4;
+                        tc_mma_bf16_ta_w(t_s, t_q + kk * 8, k_lo + ko, dhi, id_s, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ko = ((kk >> 2) * kBwdTile * 128 + (kk & 3) * 32) >> 4;
+                        tc_mma_bf16_ta_w(t_s + 64, t_q + D / 2 + kk * 8, k_lo + kK2Lo + ko, dhi, id_s, kk > 0);
+                    }
+                    tc_commit(base + L::bar_sfull);
+                    if (++s == NST) {
+                        s = 0;
+                        ph ^= 1;
+                        k_lo = k_lo0;
+                    } else {
+                        k_lo += kStageLo;
+                    }
+                }
             }
-            if (*abort_flag && started) {  // let the issued MMAs retire before TMEM is freed
+            if (*abort_flag && started) {  // let the issued copies and MMAs retire before TMEM is freed
+                tc_commit(base + L::bar_drain);
+                drain_wait_b(base + L::bar_drain, 0, kDrainNs);
+            }
+        }
+    } else if (warp == kQJointThreads / 32 - 1) {
+        // ------------------------------------------------ dQ MMAs
+        // tile it's dS (from the update warps) -> dQ1 += dS1 K1, dQ2 += dS2 K2
+        // (each dS = hi + lo); then the tile's dS buffer and key stage are
+        // released.  (Tile it's scores finished before its dS existed, so the
+        // stage's release also covers the score MMAs that read it.)
+        if (lane == 0) {
+            constexpr uint32_t id_dq = idesc_bf16_f32(kBlockQ, D, 0, 1);
+            const uint32_t t_dq1 = tmem + 256, t_dq2 = tmem + 384;
+            const uint32_t dhi = smem_desc_hi();
+            constexpr uint32_t kStageLo = (2 * L::kKBytes) >> 4, kK2Lo = L::kKBytes >> 4;
+            // B of dQ_t = K_t, MN-major: K1 at the stage, K2 right after it
+            const uint32_t kmn_lo0 = smem_desc_lo_mn128(base + L::k, kBwdTile * 128);
+            const uint32_t ds_lo[2] = {smem_desc_lo_k128(base + L::ds0), smem_desc_lo_k128(base + L::ds1)};
+            int issued = 0, s = 0;
+            uint32_t kmn_lo = kmn_lo0;
+            for (int it = 0; it < n_tiles; ++it) {
+                const int dsb = it & 1;
+                if (!mbar_wait(base + L::bar_dsfull + 8 * dsb, (it >> 1) & 1, wc, kErrWaitOther)) break;
+                tc_fence_after();
+                const uint32_t dl = ds_lo[dsb];
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < kBwdTile / 16; ++kk)
+                        tc_mma_bf16_w(t_dq1, dl + ((part * L::kDsBytes + kk * 32) >> 4), dhi,
+                                      kmn_lo + ((kk * 16 * 128) >> 4), dhi, id_dq, (it | kk | part) != 0);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < kBwdTile / 16; ++kk)
+                        tc_mma_bf16_w(t_dq2, dl + (((2 + part) * L::kDsBytes + kk * 32) >> 4), dhi,
+                                      kmn_lo + kK2Lo + ((kk * 16 * 128) >> 4), dhi, id_dq, (it | kk | part) != 0);
+                tc_commit(base + L::bar_dsempty + 8 * dsb);
+                tc_commit(base + L::bar_kempty + 8 * s);
+                if (++s == NST) {
+                    s = 0;
+                    kmn_lo = kmn_lo0;
+                } else {
+                    kmn_lo += kStageLo;
+                }
+                ++issued;
+            }
+            if (issued == n_tiles) tc_commit(base + L::bar_done);
+            if (*abort_flag && issued > 0) {  // let the issued MMAs retire before TMEM is freed
                 tc_commit(base + L::bar_done);
                 drain_wait_b(base + L::bar_done, 0, kDrainNs);
             }
@@ -230,22 +271,20 @@ __global__ void __launch_bounds__(320, 1)
                      nlb = make_float2(-lb, -lb), nxb = make_float2(-xb, -xb),
                      gs = make_float2(g * p.scale, g * p.scale);
         const int limit = p.causal ? min(i + p.diag_off, p.Nk - 1) : p.Nk - 1;
-        const uint32_t dss = base + L::ds;
         bool ok = true;
         for (int it = 0; it < n_tiles; ++it) {
-            const int buf = it & 1;
-            if (!wait_all(base + L::bar_sfull + 8 * buf, (it >> 1) & 1, wc, kErrWaitS)) {
+            if (!wait_all(base + L::bar_sfull, it & 1, wc, kErrWaitS)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t t1 = tl + buf * 128 + wg * 32, t2 = t1 + 64;
+            const uint32_t t1 = tl + 128 + wg * 32, t2 = t1 + 64;
             float z1[32], z2[32];
             tmem_ld32(t1, z1);
             tmem_ld32(t2, z2);
             tc_wait_ld();
             tc_fence_before();
-            mbar_arrive(base + L::bar_sempty + 8 * buf);
+            mbar_arrive(base + L::bar_sempty);  // the next score tile may overwrite S now
             const int last = limit - (it * kBwdTile + wg * 32);
             float v1[32], v2[32];
 #pragma unroll
@@ -263,14 +302,16 @@ __global__ void __launch_bounds__(320, 1)
                 for (int e = 0; e < 32; ++e)
                     if (e > last) v1[e] = v2[e] = 0.f;
             }
-            if (!wait_all(base + L::bar_dsempty, (it & 1) ^ 1, wc, kErrWaitOther)) {
+            const int dsb = it & 1;
+            if (!wait_all(base + L::bar_dsempty + 8 * dsb, ((it >> 1) & 1) ^ 1, wc, kErrWaitOther)) {
                 ok = false;
                 break;
             }
+            const uint32_t dss = base + (dsb ? L::ds1 : L::ds0);
             store_ds_chunk(dss, dss + L::kDsBytes, row, wg * 4, v1);
             store_ds_chunk(dss + 2 * L::kDsBytes, dss + 3 * L::kDsBytes, row, wg * 4, v2);
             fence_proxy_async_smem();
-            mbar_arrive(base + L::bar_dsfull);
+            mbar_arrive(base + L::bar_dsfull + 8 * dsb);
         }
         // epilogue: dQ1 and dQ2 rows (the scale is in dS); each warpgroup writes half the columns
         if (ok && wait_all(base + L::bar_done, 0, wc, kErrWaitOther)) {
@@ -671,7 +712,7 @@ cudaError_t set_smem(K kernel, int bytes) {
 template <int D>
 cudaError_t launch_joint_impl(const CUtensorMap* qm, const CUtensorMap* kvm, const BwdParams& pq,
                               const BwdParams& pkv, int ctas_q, int ctas_kv, cudaStream_t st) {
-    constexpr int NQ = D == 128 ? 3 : 6;
+    constexpr int NQ = D == 128 ? 3 : 4;
     constexpr int NKV = D == 128 ? 3 : 4;
     static_assert(QJointSmem<D, NQ>::alloc <= 232448, "shared memory");
     static_assert(KvJointSmem<D, NKV>::alloc <= 232448, "shared memory");
@@ -680,7 +721,7 @@ cudaError_t launch_joint_impl(const CUtensorMap* qm, const CUtensorMap* kvm, con
     cudaError_t e = set_smem(kq, QJointSmem<D, NQ>::alloc);
     if (e != cudaSuccess) return e;
     if ((e = set_smem(kkv, KvJointSmem<D, NKV>::alloc)) != cudaSuccess) return e;
-    kq<<<ctas_q, 320, QJointSmem<D, NQ>::alloc, st>>>(qm[0], qm[1], qm[2], qm[3], pq);
+    kq<<<ctas_q, kQJointThreads, QJointSmem<D, NQ>::alloc, st>>>(qm[0], qm[1], qm[2], qm[3], pq);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     kkv<<<ctas_kv, kKvJointThreads, KvJointSmem<D, NKV>::alloc, st>>>(kvm[0], kvm[1], kvm[2], kvm[3], pkv);
     return cudaGetLastError();
