@@ -90,6 +90,9 @@ WORKLOADS = {
     "8k_causal_d64": Workload("8k_causal_d64", 1, 32, 8192, 8192, 64, 0.3, True, seed=6),
     "64k_causal_d64": Workload("64k_causal_d64", 1, 32, 65536, 65536, 64, 0.3, True, seed=6),
     "512k_causal": Workload("512k_causal", 1, 8, 524288, 524288, 128, 0.3, True, teacher_scale=1.5, seed=4),
+    # 4 heads of the 64K causal workload (same seed and per-head shape; 0.5 GiB of inputs, more
+    # than L2): a DRAM-counter capture of it, times 8, gives the 32-head figure
+    "64k_causal_h4": Workload("64k_causal_h4", 1, 4, 65536, 65536, 128, 0.3, True, seed=2),
     # 64K causal with keys shared by groups of 4 query heads (32 query heads, 8 key heads)
     "64k_causal_gqa": Workload("64k_causal_gqa", 1, 32, 65536, 65536, 128, 0.3, True, seed=9, H_kv=8),
 }

@@ -6,6 +6,7 @@ Functions mirror the C ABI in ``include/streamkl.h``:
 
     kl_fwd(Q1, K1, Q2, K2, causal=False, scale=None) -> (KL, LSE1, LSE2)
     kl_bwd(setting, g, Q1, K1, Q2, K2, KL, LSE1, LSE2, causal=False) -> (dQ, dK)
+    kl_bwd_joint(g, Q1, K1, Q2, K2, KL, LSE1, LSE2, causal=False) -> (dQ1, dK1, dQ2, dK2)
 
 plus ``fwd_plan`` / ``bwd_plan`` (what a call launches) and ``AttentionKL``,
 an autograd Function.  There is no fallback: without the compiled library
@@ -333,11 +334,14 @@ class AttentionKL(torch.autograd.Function):
     """Per-row KL(softmax(Q1 K1^T s) || softmax(Q2 K2^T s)) with a recompute
     backward.  Gradients flow to the student (setting 1) or the teacher
     (setting 2), chosen by which inputs require grad; the other side gets
-    None.  When both sides require grad, both settings run, one backward pass
-    each (no fused joint pass: it would not be faster on this hardware).
-    Together they are the gradient of KL with respect to all four inputs: each
-    setting differentiates through one side's distribution with the other
-    side's held fixed.  Gradients come back in bf16, like the inputs."""
+    None.  When both sides require grad, the joint backward forms the
+    gradients of both from one recompute of the scores per kernel
+    (streamkl_bwd_joint): measured on GB300 at 64K causal it takes as long as
+    the two single-setting passes (145.7 vs 144.5 ms) and, adding no gradient
+    through atomics, gives the same bits on every run.  Together the two sides
+    are the gradient of KL with respect to all four inputs: each setting
+    differentiates through one side's distribution with the other side's held
+    fixed.  Gradients come back in bf16, like the inputs."""
 
     @staticmethod
     def forward(ctx, Q1, K1, Q2, K2, causal=False, scale=None):
@@ -354,10 +358,13 @@ class AttentionKL(torch.autograd.Function):
         if not (student or teacher):
             return (None,) * 6
         g = gKL.float().contiguous()
+        if student and teacher:
+            dQ1, dK1, dQ2, dK2 = kl_bwd_joint(g, Q1, K1, Q2, K2, KL, L1, L2, causal=ctx.causal, scale=ctx.scale,
+                                              grad_dtype=torch.bfloat16)
+            return dQ1, dK1, dQ2, dK2, None, None
         grads = [None] * 6
-        for setting, want, slot in ((1, student, 2), (2, teacher, 0)):
-            if want:
-                dQ, dK = kl_bwd(setting, g, Q1, K1, Q2, K2, KL, L1, L2, causal=ctx.causal, scale=ctx.scale,
-                                grad_dtype=torch.bfloat16)
-                grads[slot], grads[slot + 1] = dQ, dK
+        setting, slot = (1, 2) if student else (2, 0)
+        dQ, dK = kl_bwd(setting, g, Q1, K1, Q2, K2, KL, L1, L2, causal=ctx.causal, scale=ctx.scale,
+                        grad_dtype=torch.bfloat16)
+        grads[slot], grads[slot + 1] = dQ, dK
         return tuple(grads)

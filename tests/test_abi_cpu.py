@@ -88,3 +88,27 @@ def test_workspace_size_queries_reject_invalid_shapes_without_device():
     assert lib.streamkl_fwd_workspace_bytes(ctypes.byref(_shape(Nq=300, Nk=200)), 1) == 0
     assert lib.streamkl_bwd_workspace_bytes(ctypes.byref(_shape()), 3, 0) == 0  # no setting 3
     assert lib.streamkl_bwd_workspace_bytes(ctypes.byref(_shape(B=0)), 1, 0) == 0
+
+
+def test_joint_backward_rejects_bad_arguments_without_device():
+    lib = sk.load()
+    P = ctypes.c_void_p
+
+    def call(shape, ptrs=(256,) * 12, ws=256, ws_bytes=4096, causal=0):
+        # g, Q1, K1, Q2, K2, KL, LSE1, LSE2 | dQ1, dK1, dQ2, dK2
+        return lib.streamkl_bwd_joint(ctypes.byref(shape) if shape is not None else None,
+                                      *[P(p) for p in ptrs[:8]], ctypes.c_float(0.0), causal,
+                                      *[P(p) for p in ptrs[8:]], P(ws), ws_bytes, None, P(0))
+
+    assert call(None) == sk.ERR_INVALID_ARG
+    assert call(_shape(d=96)) == sk.ERR_UNSUPPORTED
+    assert call(_shape(Nq=300, Nk=200), causal=1) == sk.ERR_INVALID_ARG
+    bad = list((256,) * 12)
+    bad[11] = 0  # dK2 missing
+    assert call(_shape(), ptrs=tuple(bad)) == sk.ERR_INVALID_ARG
+    bad[11] = 264  # dK2 not 16-byte aligned
+    assert call(_shape(), ptrs=tuple(bad)) == sk.ERR_INVALID_ARG
+    bad = list((256,) * 12)
+    bad[0] = 258  # g not 4-byte aligned
+    assert call(_shape(), ptrs=tuple(bad)) == sk.ERR_INVALID_ARG
+    assert call(_shape(), ws=0) == sk.ERR_WORKSPACE

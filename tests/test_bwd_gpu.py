@@ -283,9 +283,22 @@ def test_binding_rejects_mis_shaped_buffers():
     assert torch.isfinite(dQ).all() and torch.isfinite(dK).all()
 
 
+def test_autograd_teacher_side():
+    Q1, K1, Q2, K2 = make_qk(1, 2, 200, 330, 128, 0.5, seed=3, device=DEV)
+    Q1.requires_grad_(True)
+    K1.requires_grad_(True)
+    KL = streamkl.AttentionKL.apply(Q1, K1, Q2, K2, True, None)
+    KL.sum().backward()
+    assert Q2.grad is None and K2.grad is None
+    rdQ, rdK = oracle.bwd(2, np.ones((1, 2, 200)), Q1.detach(), K1.detach(), Q2, K2, causal=True)
+    assert_grad(Q1.grad.float(), rdQ, "dQ1 (autograd)")
+    assert_grad(K1.grad.float(), rdK, "dK1 (autograd)")
+
+
 def test_autograd_both_sides():
-    """Teacher and student both require grad: each side gets its own
-    setting's gradient (setting 1 holds P1 fixed, setting 2 holds P2 fixed)."""
+    """Teacher and student both require grad: the joint backward gives each
+    side its own setting's gradient (setting 1 holds P1 fixed, setting 2 holds
+    P2 fixed) from one recompute per kernel."""
     Q1, K1, Q2, K2 = make_qk(1, 2, 180, 250, 64, 0.5, seed=4, device=DEV)
     for t in (Q1, K1, Q2, K2):
         t.requires_grad_(True)
