@@ -1,6 +1,7 @@
 """Extra HBM is O(N_Q): the forward needs its three [B, H, N_Q] outputs plus a
 workspace of 256 bytes (plus 20 bytes per row and key split when the key
-range is split); the backward needs only dQ and dK.  Nothing of size
+range is split); the backward needs only dQ and dK, and the joint backward
+only the four gradients of both sides.  Nothing of size
 N_Q x N_K is ever allocated (the pages' ~512 GB at 64K, 32 heads)."""
 import pytest
 import torch
@@ -32,5 +33,7 @@ def test_extra_memory_is_linear(N):
     extra_bwd, _ = peak_extra(lambda: streamkl.kl_bwd(1, g, Q1, K1, Q2, K2, KL, L1, L2, causal=True))
     grads = B * H * N * d * 4 * 2
     assert extra_bwd <= grads + 256 + SLACK
+    extra_joint, _ = peak_extra(lambda: streamkl.kl_bwd_joint(g, Q1, K1, Q2, K2, KL, L1, L2, causal=True))
+    assert extra_joint <= 2 * grads + 256 + SLACK
     # what materialising both distributions in bf16 would need
     assert 2 * B * H * N * N * 2 > 10 * (extra_fwd + extra_bwd) or N < 16384
