@@ -144,7 +144,7 @@ struct BwdPlan {
 // Mode choice.  The pages use the fused kernel (dQ through atomics) while the
 // float32 dQ buffer fits in L2 and separate kernels beyond.  Measured on
 // GB300 the fused kernel is faster at every size tried (setting 1: 8K causal
-// 1.21 vs 2.14 ms, 64K causal 71.0 vs 117.8 ms: the split pays a second
+// 1.21 vs 2.14 ms, 64K causal 73.4 vs 118.1 ms: the split pays a second
 // recompute of both score tiles, which costs more than the L2 reductions), so
 // the automatic choice is fused unless every query row of a key head fits one
 // CTA's 16 columns (the key-split kernel); the split stays selectable.
