@@ -242,7 +242,7 @@ int64_t wait_limit(const streamkl_options* opt) {
 
 extern "C" {
 
-int streamkl_version(void) { return 100; }
+int streamkl_version(void) { return 200; }  // 0.2.0: joint backward, size queries, allocation-free status
 
 const char* streamkl_status_string(streamkl_status s) {
     switch (s) {

@@ -24,7 +24,7 @@ def test_library_exports_every_declared_symbol():
     lib = sk.load()
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert lib.streamkl_version() >= 100
+    assert lib.streamkl_version() >= 200
 
 
 def test_status_strings():
