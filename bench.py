@@ -460,6 +460,24 @@ def run_gpu(args):
                 issue_copy_in(k + 1)
         stream.wait_event(read_out[(n - 1) % 2])
 
+    def copy_alone(fn, s):
+        """One step's copies in one direction, timed alone on their stream."""
+        ms = None
+        for _ in range(2):  # the second, warm, copy is the one kept
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(s)
+            with torch.cuda.stream(s):
+                fn()
+            b.record(s)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+        return ms
+
+    h2d_ms = copy_alone(lambda: [dst.copy_(src, non_blocking=True) for dst, src in zip(in_sets[1], host_in)],
+                        h2d_stream)
+    d2h_ms = copy_alone(lambda: [host_out[k].copy_(t, non_blocking=True) for k, t in out_sets[1].items()], d2h_stream)
+
     run_e2e(2)
     torch.cuda.synchronize()
     barrier(ws_)
@@ -472,7 +490,9 @@ def run_gpu(args):
     e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, ws_, dev)
     e2e = {"value": step_flops_all / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "read_back": sorted(host_out), "clocks": e2e_clk.summary()}
+           "read_back": sorted(host_out), "clocks": e2e_clk.summary(),
+           "copies_alone": {"h2d_ms": h2d_ms, "h2d_gbs": h2d / h2d_ms / 1e6, "d2h_ms": d2h_ms,
+                            "d2h_gbs": d2h / d2h_ms / 1e6}}
     kl_mean = float(host_out["KL"].double().mean())
     del in_sets, out_sets, host_in, host_out, out, ins, Q1, K1, Q2, K2, g
     torch.cuda.empty_cache()
