@@ -38,6 +38,10 @@
  *    runs everything asynchronously on the caller's stream.  Arguments are
  *    validated before anything is launched; on an error nothing is launched
  *    and no output is touched.
+ *  - streamkl_fwd, streamkl_bwd and streamkl_bwd_joint only enqueue
+ *    asynchronous work (kernels and a memset) on the caller's stream: with
+ *    buffers allocated beforehand, a sequence of them can be captured into a
+ *    CUDA graph and replayed.
  *  - Workspace: the first 256 bytes hold a device error word that kernels set
  *    (they never clear it) when a bounded wait inside them gives up.  Zero the
  *    workspace once when it is allocated; streamkl_workspace_status reads and
