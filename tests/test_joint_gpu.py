@@ -173,3 +173,19 @@ def test_joint_64k_noncausal_sampled():
     for x, y in ((dK1, f2[1]), (dK2, f1[1]), (dQ1, f2[0]), (dQ2, f1[0])):
         cos, rel = grad_report(x[0, 3:5], y[0, 3:5])
         assert cos > 0.99999 and rel < 1e-2, (cos, rel)
+
+
+@pytest.mark.parametrize("scale", [0.05, 0.3])
+def test_joint_explicit_scale_and_signed_g(scale):
+    """A softmax scale other than d^-1/2 and an upstream gradient of both
+    signs (and some zeros)."""
+    Q1, K1, Q2, K2 = make_qk(1, 2, 300, 420, 128, 0.4, seed=31, device=DEV)
+    g = torch.randn((1, 2, 300), device=DEV)
+    g[0, 0, ::7] = 0.0
+    KL, L1, L2 = streamkl.kl_fwd(Q1, K1, Q2, K2, causal=True, scale=scale)
+    grads = streamkl.kl_bwd_joint(g, Q1, K1, Q2, K2, KL, L1, L2, causal=True, scale=scale)
+    torch.cuda.synchronize()
+    r2 = oracle.bwd(2, g, Q1, K1, Q2, K2, causal=True, scale=scale)
+    r1 = oracle.bwd(1, g, Q1, K1, Q2, K2, causal=True, scale=scale)
+    for got, want, what in zip(grads, (r2[0], r2[1], r1[0], r1[1]), ("dQ1", "dK1", "dQ2", "dK2")):
+        assert_grad(got, want, f"{what} (scale {scale}, signed g)")
