@@ -430,6 +430,12 @@ def run_gpu(args):
     copied, freed = [torch.cuda.Event(), torch.cuda.Event()], [torch.cuda.Event(), torch.cuda.Event()]
     computed, read_out = [torch.cuda.Event(), torch.cuda.Event()], [torch.cuda.Event(), torch.cuda.Event()]
 
+    # per-step copy durations inside the loop, where they run beside the kernels
+    copy_ev = {"h2d": [], "d2h": []}
+
+    def timed_event():
+        return torch.cuda.Event(enable_timing=True)
+
     def issue_copy_in(k, after=None):
         slot = k % 2
         with torch.cuda.stream(h2d_stream):
@@ -437,11 +443,18 @@ def run_gpu(args):
                 h2d_stream.wait_event(after)
             if k >= 2:
                 h2d_stream.wait_event(freed[slot])  # step k-2 is done with this input set
+            t0 = timed_event()
+            t0.record(h2d_stream)
             for dst, src in zip(in_sets[slot], host_in):
                 dst.copy_(src, non_blocking=True)
             copied[slot].record(h2d_stream)
+            t1 = timed_event()
+            t1.record(h2d_stream)
+            copy_ev["h2d"].append((t0, t1))
 
     def run_e2e(n, start_ev=None):
+        copy_ev["h2d"].clear()
+        copy_ev["d2h"].clear()
         issue_copy_in(0, after=start_ev)
         for k in range(n):
             slot = k % 2
@@ -453,9 +466,14 @@ def run_gpu(args):
             computed[slot].record(stream)
             with torch.cuda.stream(d2h_stream):
                 d2h_stream.wait_event(computed[slot])
+                t0 = timed_event()
+                t0.record(d2h_stream)
                 for key, t in out_sets[slot].items():
                     host_out[key].copy_(t, non_blocking=True)
                 read_out[slot].record(d2h_stream)
+                t1 = timed_event()
+                t1.record(d2h_stream)
+                copy_ev["d2h"].append((t0, t1))
             if k + 1 < n:
                 issue_copy_in(k + 1)
         stream.wait_event(read_out[(n - 1) % 2])
@@ -488,11 +506,14 @@ def run_gpu(args):
         b.record(stream)
         torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, ws_, dev)
+    in_loop = {d: statistics.median(x.elapsed_time(y) for x, y in copy_ev[d]) for d in ("h2d", "d2h")}
     e2e = {"value": step_flops_all / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "read_back": sorted(host_out), "clocks": e2e_clk.summary(),
            "copies_alone": {"h2d_ms": h2d_ms, "h2d_gbs": h2d / h2d_ms / 1e6, "d2h_ms": d2h_ms,
-                            "d2h_gbs": d2h / d2h_ms / 1e6}}
+                            "d2h_gbs": d2h / d2h_ms / 1e6},
+           "copies_in_loop": {"h2d_ms": in_loop["h2d"], "h2d_gbs": h2d / in_loop["h2d"] / 1e6,
+                              "d2h_ms": in_loop["d2h"], "d2h_gbs": d2h / in_loop["d2h"] / 1e6}}
     kl_mean = float(host_out["KL"].double().mean())
     del in_sets, out_sets, host_in, host_out, out, ins, Q1, K1, Q2, K2, g
     torch.cuda.empty_cache()
