@@ -38,5 +38,6 @@ def test_bench_line_on_8k_causal():
     assert e2e["d2h_bytes_per_step"] == 3 * 32 * 8192 * 4 + 4 * 32 * 8192 * 128 * 4  # KL, LSEs, four gradients
     assert e2e["value"] > 0 and e2e["value"] <= d["value"] * 1.05
     assert e2e["copies_alone"]["h2d_gbs"] > 0 and e2e["copies_alone"]["d2h_gbs"] > 0
+    assert e2e["copies_in_loop"]["h2d_ms"] > 0 and e2e["copies_in_loop"]["d2h_ms"] > 0
     assert d["bwd_joint"]["ms"] > 0 and d["bwd_joint"]["launches"] == 2
     assert d["clocks"]["sm_mhz"] is None or d["clocks"]["sm_mhz"] > 0
