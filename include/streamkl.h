@@ -135,6 +135,21 @@ STREAMKL_API streamkl_status streamkl_fwd(const streamkl_shape* shape, const voi
 STREAMKL_API streamkl_status streamkl_bwd_plan(const streamkl_shape* shape, int setting, int causal,
                                   const streamkl_options* opt, streamkl_plan* plan);
 
+/* Backward (Methodology 2).  Gradient of sum_i g[i] * KL[i] with respect to
+ * the trainable side:
+ *   setting 1 (teacher fixed): dQ = dL/dQ2, dK = dL/dK2, dS2 = g (P2 - P1)
+ *   setting 2 (student fixed): dQ = dL/dQ1, dK = dL/dK1,
+ *                              dS1 = g P1 ((S1 - LSE1) - (S2 - LSE2) - KL)
+ * and dQ = scale * dS K, dK = scale * dS^T Q.  KL, LSE1, LSE2 are the
+ * forward's outputs for the same inputs.  dQ and dK are overwritten; they are
+ * float32 unless opt->grad_bf16 selects bf16 (the fused mode then also needs
+ * 4 bytes per dQ element of workspace to accumulate in float32).
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
+STREAMKL_API streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const float* g, const void* Q1,
+                             const void* K1, const void* Q2, const void* K2, const float* KL, const float* LSE1,
+                             const float* LSE2, float scale, int causal, void* dQ, void* dK, void* workspace,
+                             size_t workspace_bytes, const streamkl_options* opt, streamkl_stream_t stream);
+
 /* Joint backward (Methodology 2, both settings at once): the gradient of
  * sum_i g[i] * KL[i] with respect to all four inputs, where the teacher's
  * gradients differentiate through P1 with P2 held fixed (setting 2) and the
@@ -167,21 +182,6 @@ STREAMKL_API streamkl_status streamkl_bwd_joint(const streamkl_shape* shape, con
  * queries. */
 STREAMKL_API size_t streamkl_fwd_workspace_bytes(const streamkl_shape* shape, int causal);
 STREAMKL_API size_t streamkl_bwd_workspace_bytes(const streamkl_shape* shape, int setting, int causal);
-
-/* Backward (Methodology 2).  Gradient of sum_i g[i] * KL[i] with respect to
- * the trainable side:
- *   setting 1 (teacher fixed): dQ = dL/dQ2, dK = dL/dK2, dS2 = g (P2 - P1)
- *   setting 2 (student fixed): dQ = dL/dQ1, dK = dL/dK1,
- *                              dS1 = g P1 ((S1 - LSE1) - (S2 - LSE2) - KL)
- * and dQ = scale * dS K, dK = scale * dS^T Q.  KL, LSE1, LSE2 are the
- * forward's outputs for the same inputs.  dQ and dK are overwritten; they are
- * float32 unless opt->grad_bf16 selects bf16 (the fused mode then also needs
- * 4 bytes per dQ element of workspace to accumulate in float32).
- * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
-STREAMKL_API streamkl_status streamkl_bwd(const streamkl_shape* shape, int setting, const float* g, const void* Q1,
-                             const void* K1, const void* Q2, const void* K2, const float* KL, const float* LSE1,
-                             const float* LSE2, float scale, int causal, void* dQ, void* dK, void* workspace,
-                             size_t workspace_bytes, const streamkl_options* opt, streamkl_stream_t stream);
 
 /* Size of the library's own built-in scratch buffer used by streamkl_fwd_noalloc. */
 #define STREAMKL_NOALLOC_SCRATCH_BYTES (8u << 20)
