@@ -338,7 +338,9 @@ class AttentionKL(torch.autograd.Function):
     gradients of both from one recompute of the scores per kernel
     (streamkl_bwd_joint): measured on GB300 at 64K causal it takes as long as
     the two single-setting passes (145.7 vs 144.5 ms) and, adding no gradient
-    through atomics, gives the same bits on every run.  Together the two sides
+    through atomics, gives the same bits on every run.  For at most 16 query
+    rows per key head (decode shapes) the two single-setting key-split passes
+    run instead.  Together the two sides
     are the gradient of KL with respect to all four inputs: each setting
     differentiates through one side's distribution with the other side's held
     fixed.  Gradients come back in bf16, like the inputs."""
@@ -358,7 +360,9 @@ class AttentionKL(torch.autograd.Function):
         if not (student or teacher):
             return (None,) * 6
         g = gKL.float().contiguous()
-        if student and teacher:
+        # the joint pass where the single-setting backward is the fused kernel; for at most 16 query
+        # rows per key head the two key-split passes stream the keys far faster
+        if student and teacher and bwd_plan(Q1, K1, 1, causal=ctx.causal).path == PATH_BWD_FUSED:
             dQ1, dK1, dQ2, dK2 = kl_bwd_joint(g, Q1, K1, Q2, K2, KL, L1, L2, causal=ctx.causal, scale=ctx.scale,
                                               grad_dtype=torch.bfloat16)
             return dQ1, dK1, dQ2, dK2, None, None

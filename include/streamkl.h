@@ -163,7 +163,9 @@ STREAMKL_API streamkl_status streamkl_bwd(const streamkl_shape* shape, int setti
  * (opt->grad_bf16) and shared keys as for streamkl_bwd; dQ1/dQ2 are
  * [B, H, Nq, d], dK1/dK2 [B, H_kv, Nk, d].  opt->bwd_mode must be 0 and
  * num_splits is ignored.  The workspace holds the 256-byte error word only
- * (streamkl_bwd_joint_plan: path 5, 2 launches).
+ * (streamkl_bwd_joint_plan: path 5, 2 launches).  For at most 16 query rows
+ * per key head (decode shapes) two streamkl_bwd calls, which take the
+ * key-split kernel there, are faster.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA. */
 STREAMKL_API streamkl_status streamkl_bwd_joint_plan(const streamkl_shape* shape, int causal,
                                                      const streamkl_options* opt, streamkl_plan* plan);

@@ -312,3 +312,22 @@ def test_autograd_both_sides():
     assert_grad(K2.grad.float(), r1[1], "dK2 (both sides)")
     assert_grad(Q1.grad.float(), r2[0], "dQ1 (both sides)")
     assert_grad(K1.grad.float(), r2[1], "dK1 (both sides)")
+
+
+def test_autograd_both_sides_decode_shape():
+    """Both sides trainable with 8 query rows against 3000 keys: the two
+    key-split passes serve it (the joint pass is for the fused shapes)."""
+    Q1, K1, Q2, K2 = make_qk(1, 2, 8, 3000, 128, 0.5, seed=6, device=DEV)
+    assert streamkl.bwd_plan(Q1, K1, 1).path == streamkl.PATH_BWD_KEYSPLIT
+    for t in (Q1, K1, Q2, K2):
+        t.requires_grad_(True)
+    KL = streamkl.AttentionKL.apply(Q1, K1, Q2, K2, False, None)
+    g = torch.rand((1, 2, 8), device=DEV) + 0.5
+    (KL * g).sum().backward()
+    det = [t.detach() for t in (Q1, K1, Q2, K2)]
+    r1 = oracle.bwd(1, g, *det, causal=False)
+    r2 = oracle.bwd(2, g, *det, causal=False)
+    assert_grad(Q2.grad.float(), r1[0], "dQ2 (both sides, decode shape)")
+    assert_grad(K2.grad.float(), r1[1], "dK2 (both sides, decode shape)")
+    assert_grad(Q1.grad.float(), r2[0], "dQ1 (both sides, decode shape)")
+    assert_grad(K1.grad.float(), r2[1], "dK1 (both sides, decode shape)")
