@@ -367,8 +367,9 @@ class AttentionKL(torch.autograd.Function):
                                               grad_dtype=torch.bfloat16)
             return dQ1, dK1, dQ2, dK2, None, None
         grads = [None] * 6
-        setting, slot = (1, 2) if student else (2, 0)
-        dQ, dK = kl_bwd(setting, g, Q1, K1, Q2, K2, KL, L1, L2, causal=ctx.causal, scale=ctx.scale,
-                        grad_dtype=torch.bfloat16)
-        grads[slot], grads[slot + 1] = dQ, dK
+        for setting, want, slot in ((1, student, 2), (2, teacher, 0)):
+            if want:
+                dQ, dK = kl_bwd(setting, g, Q1, K1, Q2, K2, KL, L1, L2, causal=ctx.causal, scale=ctx.scale,
+                                grad_dtype=torch.bfloat16)
+                grads[slot], grads[slot + 1] = dQ, dK
         return tuple(grads)
