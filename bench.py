@@ -431,7 +431,7 @@ def run_gpu(args):
     computed, read_out = [torch.cuda.Event(), torch.cuda.Event()], [torch.cuda.Event(), torch.cuda.Event()]
 
     # per-step copy durations inside the loop, where they run beside the kernels
-    copy_ev = {"h2d": [], "d2h": []}
+    copy_ev = {"h2d": [], "d2h": [], "compute": []}
 
     def timed_event():
         return torch.cuda.Event(enable_timing=True)
@@ -453,15 +453,20 @@ def run_gpu(args):
             copy_ev["h2d"].append((t0, t1))
 
     def run_e2e(n, start_ev=None):
-        copy_ev["h2d"].clear()
-        copy_ev["d2h"].clear()
+        for v in copy_ev.values():
+            v.clear()
         issue_copy_in(0, after=start_ev)
         for k in range(n):
             slot = k % 2
             stream.wait_event(copied[slot])
             if k >= 2:
                 stream.wait_event(read_out[slot])  # step k-2's outputs have been copied out
+            c0 = timed_event()
+            c0.record(stream)
             step_on(in_sets[slot], out_sets[slot])
+            c1 = timed_event()
+            c1.record(stream)
+            copy_ev["compute"].append((c0, c1))
             freed[slot].record(stream)
             computed[slot].record(stream)
             with torch.cuda.stream(d2h_stream):
@@ -506,14 +511,15 @@ def run_gpu(args):
         b.record(stream)
         torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, ws_, dev)
-    in_loop = {d: statistics.median(x.elapsed_time(y) for x, y in copy_ev[d]) for d in ("h2d", "d2h")}
+    in_loop = {d: statistics.median(x.elapsed_time(y) for x, y in copy_ev[d]) for d in ("h2d", "d2h", "compute")}
     e2e = {"value": step_flops_all / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "read_back": sorted(host_out), "clocks": e2e_clk.summary(),
            "copies_alone": {"h2d_ms": h2d_ms, "h2d_gbs": h2d / h2d_ms / 1e6, "d2h_ms": d2h_ms,
                             "d2h_gbs": d2h / d2h_ms / 1e6},
            "copies_in_loop": {"h2d_ms": in_loop["h2d"], "h2d_gbs": h2d / in_loop["h2d"] / 1e6,
-                              "d2h_ms": in_loop["d2h"], "d2h_gbs": d2h / in_loop["d2h"] / 1e6}}
+                              "d2h_ms": in_loop["d2h"], "d2h_gbs": d2h / in_loop["d2h"] / 1e6},
+           "kernels_in_loop_ms": in_loop["compute"]}
     kl_mean = float(host_out["KL"].double().mean())
     del in_sets, out_sets, host_in, host_out, out, ins, Q1, K1, Q2, K2, g
     torch.cuda.empty_cache()
