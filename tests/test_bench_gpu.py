@@ -39,5 +39,6 @@ def test_bench_line_on_8k_causal():
     assert e2e["value"] > 0 and e2e["value"] <= d["value"] * 1.05
     assert e2e["copies_alone"]["h2d_gbs"] > 0 and e2e["copies_alone"]["d2h_gbs"] > 0
     assert e2e["copies_in_loop"]["h2d_ms"] > 0 and e2e["copies_in_loop"]["d2h_ms"] > 0
+    assert e2e["kernels_in_loop_ms"] > 0
     assert d["bwd_joint"]["ms"] > 0 and d["bwd_joint"]["launches"] == 2
     assert d["clocks"]["sm_mhz"] is None or d["clocks"]["sm_mhz"] > 0
