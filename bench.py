@@ -159,12 +159,20 @@ def gpu_id(dev):
         return str(dev.index or 0)
 
 
+L2_BYTES = 129 * 2**20  # GB300 L2
+
+
+def input_bytes(w):
+    """bf16 Q1, K1, Q2, K2 of the whole workload."""
+    return 2 * 2 * w.d * w.B * (w.H * w.Nq + (w.H_kv or w.H) * w.Nk)
+
+
 def config_for(w, world):
     return {"workload": f"{w.name}: B={w.B} H={w.H}{f' H_kv={w.H_kv}' if w.H_kv else ''} N_Q={w.Nq} N_K={w.Nk} d={w.d} "
                         f"{'causal' if w.causal else 'non-causal'}, "
                         + ("fwd only (Split-K decode) per step" if w.fwd_only else
                            "fwd + bwd setting 1 + bwd setting 2 per step"),
-            "l2": "256 MB write between steps (inputs exceed L2 as well)",
+            "l2": "256 MB write between steps" + (" (inputs exceed L2 as well)" if input_bytes(w) > L2_BYTES else ""),
             "parallelism": f"heads split across {world} GPU(s), no collective on the data path"}
 
 
